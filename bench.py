@@ -1,0 +1,397 @@
+"""SGEMM throughput benchmark (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one C = alpha*A*B + beta*C call on the workload (default: the
+M = N = K = 4096 cube, uniform[-1, 1] inputs from seed 1, alpha = 0.5,
+beta = 3). Inputs are resident on the device before timing; A + B + C
+(201 MB at 4096) exceed the 129 MB L2, so no flush is needed between steps.
+`value` is GFLOP/s (2*M*N*K per step) over exactly K timed steps bracketed by
+a barrier and a device synchronisation, max over ranks; N > 1 runs
+independent replicas (the path has no exchange step). `e2e` times the same
+work from pinned host buffers: H2D of A, B, C, the call, D2H of C.
+`--impl reference` times the CPU oracle (FP64 triple loop) on a bounded row
+sample of the same workload; it runs on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import glob
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM GFLOP/s at M=N=K=4096 FP32 and % of GB300 FP32 FFMA peak (1 GPU)"
+UNIT = "GFLOP/s"
+FFMA_FLOP_PER_CLK_PER_SM = 256  # 128 FP32 lanes x 2 FLOP per fused multiply-add
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---- accounting (checked against the pages' printed numbers in tests) -------------
+def gemm_flops(M, N, K):
+    return 2 * M * N * K
+
+
+def gflops(M, N, K, seconds):
+    return gemm_flops(M, N, K) / seconds / 1e9
+
+
+def gmem_accesses_per_result(K, BM, BN):
+    """Global loads per output element for a BM x BN tile: K*(1/BM + 1/BN)."""
+    return K * (1.0 / BM + 1.0 / BN)
+
+
+def smem_loads_per_result(K, TM, TN):
+    """Shared loads per output element for a TM x TN thread tile."""
+    return K * (1.0 / TM + 1.0 / TN)
+
+
+def min_bytes(M, N, K, beta):
+    """Algorithmic bytes: read A and B once, write C (and read it if beta != 0)."""
+    return 4 * (M * K + K * N + M * N * (2 if beta != 0 else 1))
+
+
+def ffma_peak_tflops(sms, mhz):
+    return sms * mhz * 1e6 * FFMA_FLOP_PER_CLK_PER_SM / 1e12
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_gemm_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return {}
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    or None if there is none or the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", f"ffma_sgemm_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---- clocks -------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sgemm_clocks_{os.getpid()}.csv")
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mhz = sorted(r[1] for r in inside)
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4]) if v == "Active"})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in inside),
+                "samples": len(inside), "reasons": reasons}
+
+
+# ---- distributed helpers (replicas only) ------------------------------------------
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(flops_per_step_per_rank, steps, seconds_max, world):
+    """Whole-job throughput: work of all ranks over the slowest rank's time."""
+    return flops_per_step_per_rank * steps * world / seconds_max / 1e9
+
+
+# ---- CPU oracle timing --------------------------------------------------------------
+def oracle_rows_timing(w, A, B, C, rows, threads):
+    import oracle
+    Cn = None if w.beta == 0 else C.numpy()
+    t0 = time.perf_counter()
+    oracle.sgemm_rows(w.M, w.N, w.K, w.alpha, A.numpy(), w.LDA, B.numpy(), w.LDB, w.beta, Cn,
+                      w.LDC, 0, rows, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, A, B, C, budget_s=10.0):
+    """The oracle as it stands, on the host cores, over a growing row sample
+    until about budget_s of CPU work has been timed."""
+    threads = len(os.sched_getaffinity(0))
+    rows, spent, total_rows = max(1, threads), 0.0, 0
+    while True:
+        rows = min(rows, w.M)
+        dt = oracle_rows_timing(w, A, B, C, rows, threads)
+        if dt >= budget_s / 4 or rows == w.M:
+            spent, total_rows = dt, rows
+            break
+        rows = min(w.M, max(rows * 2, int(rows * (budget_s / 4) / max(dt, 1e-3))))
+    value = gemm_flops(total_rows, w.N, w.K) / spent / 1e9
+    return {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {total_rows} of {w.M} rows of C ({w.N} columns, K={w.K}), "
+                      f"{spent:.2f} s, FP64 i-j-k loop, rows split over {threads} threads"}
+
+
+# ---- arms ---------------------------------------------------------------------------
+def run_reference(args, w):
+    """Times the oracle (the CPU reference arm) on bounded row samples."""
+    from dense_fp32_gemm_gb300.workloads import make_inputs
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return None
+    A, B, C = make_inputs(w)
+    threads = len(os.sched_getaffinity(0))
+    # rows per step so that one step costs about 0.2 s of host time
+    t = oracle_rows_timing(w, A, B, C, threads, threads)
+    rows = max(1, min(w.M, int(threads * 0.2 / max(t, 1e-4))))
+    for _ in range(args.warmup):
+        oracle_rows_timing(w, A, B, C, rows, threads)
+    spent = sum(oracle_rows_timing(w, A, B, C, rows, threads) for _ in range(args.steps))
+    value = gemm_flops(rows, w.N, w.K) * args.steps / spent / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(spent / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} rows of C per step ({w.N} columns, K={w.K})"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    return line
+
+
+def workload_config(w):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "lda": w.LDA, "ldb": w.LDB,
+            "ldc": w.LDC, "alpha": w.alpha, "beta": w.beta, "dist": w.dist, "seed": w.seed,
+            "layout": "row-major",
+            "l2": ("inputs larger than L2" if min_bytes(w.M, w.N, w.K, 1) > L2_BYTES
+                   else "inputs smaller than L2 (no flush)")}
+
+
+def run_ours(args, w):
+    import torch
+
+    from dense_fp32_gemm_gb300 import binding
+    from dense_fp32_gemm_gb300.workloads import make_inputs
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+
+    A, B, C = make_inputs(w)
+    dA, dB, dC = A.to(dev), B.to(dev), C.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step():
+        st = binding.sgemm(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(), w.LDB,
+                           w.beta, dC.data_ptr(), w.LDC, sh)
+        if st != 0:
+            raise RuntimeError(f"sgemm: {binding.sgemm_status_string(st)}")
+
+    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    gpu_id = visible[local] if local < len(visible) else str(local)
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    time.sleep(1.0 if sampler else 0.0)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st, detail = binding.sgemm_poll_device_status(sh)
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail} after warm-up")
+
+    # ---- timed region: exactly K steps -------------------------------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_wall1 = time.time()
+    total_s = start.elapsed_time(end) / 1e3
+    kern_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / args.steps
+    if sampler:
+        sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    st, detail = binding.sgemm_poll_device_status(sh)
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {detail} after timing")
+    tile_config = binding.sgemm_last_config()
+    total_max = max_over_ranks(total_s, world)
+    value = aggregate(gemm_flops(w.M, w.N, w.K), args.steps, total_max, world)
+
+    # ---- end to end from pinned host buffers --------------------------------------
+    e2e_steps = max(3, min(args.steps, 20))
+    hA, hB, hC = A.pin_memory(), B.pin_memory(), C.pin_memory()
+    hg = binding.HostGemm(w.M, w.N, w.K, device=dev)
+    hA2, hB2 = hA.view(w.M, w.LDA), hB.view(w.K, w.LDB)
+    hC2 = hC.view(w.M, w.LDC)
+    for _ in range(2):
+        hg(hA2, hB2, hC2.clone().pin_memory(), w.alpha, w.beta)
+    torch.cuda.synchronize(dev)
+    out = hC2.clone().pin_memory()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        hg(hA2, hB2, out, w.alpha, w.beta)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = aggregate(gemm_flops(w.M, w.N, w.K), e2e_steps, e2e_s, world)
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    max_mhz = float(peaks.get("sm_max_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0)
+    peak_tf = ffma_peak_tflops(sms, max_mhz)
+    achieved_tf = gemm_flops(w.M, w.N, w.K) / kern_s / 1e12
+    traffic = profiled_traffic(w.name)
+    sampled = (clocks or {}).get("sm_mhz")
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_max / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(w), parallelism=f"replicas{world}",
+                       tile_config=tile_config),
+        "pct_of_ffma_peak": round(100 * achieved_tf / peak_tf, 2),
+        "pct_of_ffma_peak_at_sampled_clock": (round(100 * achieved_tf / ffma_peak_tflops(sms, sampled), 2)
+                                              if sampled else None),
+        "roofline": {"bound": "alu", "achieved": round(achieved_tf, 3), "peak": round(peak_tf, 3),
+                     "unit": "TFLOP/s", "frac": round(achieved_tf / peak_tf, 4),
+                     "traffic": traffic,
+                     "peak_basis": f"{sms} SMs x {max_mhz:.0f} MHz x 128 FFMA/clk x 2 "
+                                   "(FP32 pipe; clock from MEASURED_PEAKS.json sm_max_mhz)",
+                     "kernel_ms": round(kern_s * 1e3, 4)},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT,
+                "h2d_bytes_per_step": hg.h2d_bytes(w.beta), "d2h_bytes_per_step": hg.d2h_bytes(),
+                "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, A, B, C, budget_s=args.cpu_budget)
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="square4096")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from dense_fp32_gemm_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+"""ctypes binding of libsgemm_gb300.so: the C ABI of include/sgemm_gb300.h
+under the same names, plus two torch conveniences that only marshal arguments
+(device tensors -> pointers and leading dimensions, the current stream).
+
+There is no fallback: if the CUDA library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+SGEMM_OK = 0
+SGEMM_ERR_INVALID_DIM = -1
+SGEMM_ERR_INVALID_LD = -2
+SGEMM_ERR_NULL_PTR = -3
+SGEMM_ERR_UNSUPPORTED_DEVICE = -4
+SGEMM_ERR_LAUNCH = -5
+SGEMM_ERR_DEVICE_TIMEOUT = -6
+SGEMM_ERR_ALLOC = -7
+SGEMM_ERR_MISALIGNED = -8
+SGEMM_ERR_INVALID_VALUE = -9
+
+PARAM_NAMES = ("BM", "BN", "BK", "WM", "WN", "WNITER", "TM", "TN", "NT", "STAGES", "MINB")
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {sgemm_status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(path)
+            I, F, P, LL = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_longlong
+            IP = ctypes.POINTER(ctypes.c_int)
+            sig = {
+                "sgemm": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_status_string": (ctypes.c_char_p, [I]),
+                "sgemm_last_config": (I, [ctypes.c_char_p, I]),
+                "sgemm_poll_device_status": (I, [P, IP]),
+                "sgemm_shutdown": (None, []),
+                "sgemm_config_count": (I, []),
+                "sgemm_config_info": (I, [I, ctypes.c_char_p, I, IP]),
+                "sgemm_force_config": (I, [I]),
+                "sgemm_cfg_check": (I, [IP, IP]),
+                "sgemm_schedule_query": (I, [I, I, I, I, I, IP]),
+                "sgemm_schedule_piece": (I, [IP, I, I, IP]),
+                "sgemm_diag_wait_timeout": (I, [LL, P]),
+                "sgemm_set_wait_timeout_ns": (LL, [LL]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _ints(n, values=None):
+    arr = (ctypes.c_int * n)()
+    if values is not None:
+        for i, v in enumerate(values):
+            arr[i] = int(v)
+    return arr
+
+
+# ---- the C ABI, same names ------------------------------------------------------
+def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """Raw call: A, B, C are device addresses (ints), stream a cudaStream_t
+    handle (int) or None. Returns the status code."""
+    return lib().sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_status_string(status: int) -> str:
+    return lib().sgemm_status_string(status).decode()
+
+
+def sgemm_last_config() -> str:
+    buf = ctypes.create_string_buffer(256)
+    lib().sgemm_last_config(buf, 256)
+    return buf.value.decode()
+
+
+def sgemm_poll_device_status(stream=None):
+    """(status, device detail code)."""
+    detail = ctypes.c_int(0)
+    st = lib().sgemm_poll_device_status(stream, ctypes.byref(detail))
+    return st, detail.value
+
+
+def sgemm_shutdown() -> None:
+    lib().sgemm_shutdown()
+
+
+def sgemm_config_count() -> int:
+    return lib().sgemm_config_count()
+
+
+def sgemm_config_info(cid: int):
+    name = ctypes.create_string_buffer(128)
+    params = _ints(11)
+    st = lib().sgemm_config_info(cid, name, 128, params)
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_config_info")
+    return name.value.decode(), dict(zip(PARAM_NAMES, list(params)))
+
+
+def sgemm_force_config(cid: int) -> int:
+    return lib().sgemm_force_config(cid)
+
+
+def sgemm_cfg_check(params):
+    """(rule, derived): rule 0 = legal; derived = {WMITER, WSUBM, WSUBN,
+    acc_per_thread, smem_bytes} for a legal tuple."""
+    if isinstance(params, dict):
+        params = [params[k] for k in PARAM_NAMES]
+    p = _ints(11, params)
+    d = _ints(5)
+    rule = lib().sgemm_cfg_check(p, d)
+    derived = dict(zip(("WMITER", "WSUBM", "WSUBN", "acc", "smem_bytes"), list(d))) if rule == 0 else None
+    return rule, derived
+
+
+SCHED_FIELDS = ("tiles_m", "tiles_n", "kiters", "grid", "dp_tiles", "sk_q", "sk_r", "group_m")
+PIECE_FIELDS = ("tile", "kb", "ke", "tile_m", "tile_n", "contributors", "is_partial")
+
+
+def sgemm_schedule_query(M, N, K, cid, capacity):
+    out = _ints(8)
+    st = lib().sgemm_schedule_query(M, N, K, cid, capacity, out)
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_schedule_query")
+    return dict(zip(SCHED_FIELDS, list(out)))
+
+
+def sgemm_schedule_piece(sched: dict, b: int, i: int):
+    """(number of pieces of CTA b, piece i as a dict)."""
+    v = _ints(8, [sched[k] for k in SCHED_FIELDS])
+    out = _ints(7)
+    n = lib().sgemm_schedule_piece(v, b, i, out)
+    if n < 0:
+        raise SgemmError(n, "sgemm_schedule_piece")
+    return n, dict(zip(PIECE_FIELDS, list(out)))
+
+
+def sgemm_diag_wait_timeout(timeout_ns: int, stream=None) -> int:
+    return lib().sgemm_diag_wait_timeout(timeout_ns, stream)
+
+
+def sgemm_set_wait_timeout_ns(ns: int) -> int:
+    return lib().sgemm_set_wait_timeout_ns(ns)
+
+
+# ---- torch conveniences (marshalling only) ------------------------------------------
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ld(t, name):
+    if t.dim() != 2 or t.dtype.__repr__() != "torch.float32":
+        raise ValueError(f"{name} must be a 2-D float32 tensor")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit stride along rows)")
+    return max(t.stride(0), max(t.size(1), 1)) if t.size(0) > 1 else max(t.size(1), 1)
+
+
+def gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
+    """C <- alpha*A@B + beta*C on CUDA float32 tensors (row-major views with
+    any row stride). Raises SgemmError on a non-zero status. Returns C."""
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    for t, nm in ((A, "A"), (B, "B"), (C, "C")):
+        if not t.is_cuda:
+            raise ValueError(f"{nm} must be a CUDA tensor")
+    st = sgemm(M, N, K, float(alpha), A.data_ptr(), _ld(A, "A"), B.data_ptr(), _ld(B, "B"),
+               float(beta), C.data_ptr(), _ld(C, "C"), _stream_handle(stream))
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm")
+    return C
+
+
+class HostGemm:
+    """End-to-end SGEMM on host (pinned) matrices: copies A, B and C to
+    device buffers it keeps, calls sgemm on `stream`, copies C back. The
+    device buffers are allocated once per shape by torch."""
+
+    def __init__(self, M, N, K, device="cuda"):
+        import torch
+        self.M, self.N, self.K = M, N, K
+        self.dA = torch.empty((M, K), dtype=torch.float32, device=device)
+        self.dB = torch.empty((K, N), dtype=torch.float32, device=device)
+        self.dC = torch.empty((M, N), dtype=torch.float32, device=device)
+
+    def h2d_bytes(self, beta):
+        return 4 * (self.M * self.K + self.K * self.N + (self.M * self.N if beta != 0 else 0))
+
+    def d2h_bytes(self):
+        return 4 * self.M * self.N
+
+    def __call__(self, hA, hB, hC, alpha, beta, stream=None):
+        """hA, hB, hC: pinned host tensors; hC receives the result."""
+        self.dA.copy_(hA, non_blocking=True)
+        self.dB.copy_(hB, non_blocking=True)
+        if beta != 0:
+            self.dC.copy_(hC, non_blocking=True)
+        gemm(self.dA, self.dB, self.dC, alpha, beta, stream)
+        hC.copy_(self.dC, non_blocking=True)
+        return hC

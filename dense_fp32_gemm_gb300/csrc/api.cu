@@ -1,0 +1,441 @@
+// api.cu -- the extern "C" boundary of the library: argument validation,
+// quick returns, choice of tile configuration, TMA descriptor for B, the
+// per-(device, stream) workspace, and the launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "../../include/sgemm_gb300.h"
+#include "configs.hpp"
+#include "ffma_sgemm.cuh"
+#include "schedule.hpp"
+#include "tile_config.hpp"
+
+#define SGEMM_API extern "C" __attribute__((visibility("default")))
+
+namespace sgemm_gb300 {
+namespace {
+
+// ---- configuration registry -------------------------------------------------
+const ConfigEntry* const kConfigs[] = {&kEntryWide, &kEntryTall, &kEntrySquare, &kEntryPages};
+constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
+enum : int { kIdWide = 0, kIdTall = 1, kIdSquare = 2, kIdPages = 3 };
+
+// Raster group height (tiles) and the fewest k-slices worth splitting off.
+constexpr int kGroupM = 8;
+constexpr int kMinSplitUnits = 4;
+
+std::mutex g_mutex;
+std::atomic<int> g_forced{-1};
+std::atomic<long long> g_timeout_ns{4000000000LL};
+thread_local char g_last_config[192] = "none";
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int sms = 0;
+  int occupancy[kNumConfigs][2] = {};  // [config][tma]
+};
+std::map<int, DeviceInfo> g_devices;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+struct Workspace {
+  void* block = nullptr;
+  size_t bytes = 0;
+  int* status = nullptr;
+  uint32_t* flags = nullptr;
+  float* partials = nullptr;
+  size_t flag_cap = 0;
+  size_t partial_cap = 0;  // floats
+  uint32_t epoch = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+// Per-device set-up: compute capability check, shared-memory attributes and
+// occupancy of every configuration. Called with g_mutex held.
+int device_info(int dev, DeviceInfo** out) {
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      for (int c = 0; c < kNumConfigs; ++c) {
+        if (kConfigs[c]->set_attributes() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        for (int t = 0; t < 2; ++t) {
+          int blocks = 0;
+          if (kConfigs[c]->occupancy(t != 0, &blocks) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+          d.occupancy[c][t] = blocks;
+        }
+      }
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return d.supported ? SGEMM_OK : SGEMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// Workspace of at least `flags` flags and `partial_floats` floats for this
+// (device, stream); grows by reallocation. Called with g_mutex held.
+int get_workspace(int dev, cudaStream_t stream, size_t flags, size_t partial_floats,
+                  Workspace** out) {
+  Workspace& w = g_workspaces[{dev, stream}];
+  if (w.block == nullptr || w.flag_cap < flags || w.partial_cap < partial_floats) {
+    const size_t fcap = flags > w.flag_cap ? flags : w.flag_cap;
+    const size_t pcap = partial_floats > w.partial_cap ? partial_floats : w.partial_cap;
+    const size_t status_bytes = 256;
+    const size_t flag_bytes = ((fcap * 4 + 255) / 256) * 256;
+    const size_t bytes = status_bytes + flag_bytes + pcap * 4;
+    if (w.block != nullptr) {
+      // the old block may still be in use by queued work on this stream
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+      cudaFree(w.block);
+      w.block = nullptr;
+    }
+    void* blk = nullptr;
+    if (cudaMalloc(&blk, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      w = Workspace{};
+      return SGEMM_ERR_ALLOC;
+    }
+    if (cudaMemsetAsync(blk, 0, status_bytes + flag_bytes, stream) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    w.block = blk;
+    w.bytes = bytes;
+    w.status = static_cast<int*>(blk);
+    w.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(blk) + status_bytes);
+    w.partials = reinterpret_cast<float*>(static_cast<char*>(blk) + status_bytes + flag_bytes);
+    w.flag_cap = fcap;
+    w.partial_cap = pcap;
+  }
+  *out = &w;
+  return SGEMM_OK;
+}
+
+// Automatic choice of tile configuration by shape class.
+int choose_config(int M, int N, int K, int sms) {
+  (void)K;
+  if (N <= 96) return kIdTall;
+  const long long wide_tiles = (long long)((M + 127) / 128) * ((N + 255) / 256);
+  if (wide_tiles >= sms) return kIdWide;
+  return kIdSquare;
+}
+
+__global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {
+  const long long total = (long long)M * N;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long i = e / N, j = e % N;
+    float* c = C + i * ldc + j;
+    *c = beta == 0.f ? 0.f : beta * *c;
+  }
+}
+
+__global__ void diag_wait_kernel(int* status, long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_w;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_addr(&bar), 1);
+    abort_w = 0;
+    ptx::mbar_fence_init();
+  }
+  __syncthreads();
+  // phase 0 of `bar` never completes: nothing arrives
+  bounded_wait(ptx::smem_addr(&bar), 0u, &abort_w, status, kDevTimeoutFull, timeout_ns);
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  return SGEMM_OK;
+}
+
+}  // namespace
+}  // namespace sgemm_gb300
+
+using namespace sgemm_gb300;
+
+SGEMM_API const char* sgemm_status_string(int status) {
+  switch (status) {
+    case SGEMM_OK: return "ok";
+    case SGEMM_ERR_INVALID_DIM: return "invalid dimension (M, N or K negative)";
+    case SGEMM_ERR_INVALID_LD: return "invalid leading dimension";
+    case SGEMM_ERR_NULL_PTR: return "null matrix pointer";
+    case SGEMM_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103 (GB300)";
+    case SGEMM_ERR_LAUNCH: return "CUDA runtime error";
+    case SGEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case SGEMM_ERR_ALLOC: return "workspace allocation failed";
+    case SGEMM_ERR_MISALIGNED: return "matrix pointer not 4-byte aligned";
+    case SGEMM_ERR_INVALID_VALUE: return "invalid argument value";
+    default: return "unknown status";
+  }
+}
+
+SGEMM_API int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                    int ldb, float beta, float* C, int ldc, void* stream_) {
+  // ---- host-side validation: nothing is launched on error ------------------
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return SGEMM_ERR_INVALID_LD;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  const bool reads_ab = (K > 0 && alpha != 0.f);
+  if (C == nullptr || (reads_ab && (A == nullptr || B == nullptr))) return SGEMM_ERR_NULL_PTR;
+  if ((reinterpret_cast<uintptr_t>(C) & 3u) ||
+      (reads_ab && ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))))
+    return SGEMM_ERR_MISALIGNED;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  int st = current_device(&dev);
+  if (st != SGEMM_OK) return st;
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo* di = nullptr;
+  st = device_info(dev, &di);
+  if (st != SGEMM_OK) return st;
+
+  if (!reads_ab) {
+    // C = beta * C (beta == 0 writes zeros without reading C)
+    const long long total = (long long)M * N;
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > di->sms * 8) blocks = di->sms * 8;
+    scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    snprintf(g_last_config, sizeof(g_last_config), "scale_c");
+    return SGEMM_OK;
+  }
+
+  int id = g_forced.load();
+  if (id < 0 || id >= kNumConfigs) id = choose_config(M, N, K, di->sms);
+  const ConfigEntry& cfg = *kConfigs[id];
+  const TileShape& S = cfg.shape;
+
+  // B by TMA when its base is 16-byte aligned and its rows are 16-byte strided
+  bool tma = ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) && ((ldb & 3) == 0);
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (tma) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    tma = false;
+    if (enc != nullptr) {
+      cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+      cuuint64_t strides[1] = {(cuuint64_t)ldb * 4};
+      cuuint32_t box[2] = {(cuuint32_t)S.BN, (cuuint32_t)S.BK};
+      cuuint32_t estr[2] = {1, 1};
+      CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims,
+                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      tma = (r == CUDA_SUCCESS);
+    }
+  }
+
+  const int occ = di->occupancy[id][tma ? 1 : 0];
+  if (occ < 1) return SGEMM_ERR_LAUNCH;
+  const int tiles_m = (M + S.BM - 1) / S.BM, tiles_n = (N + S.BN - 1) / S.BN;
+  const int kiters = (K + S.BK - 1) / S.BK;
+  Schedule sched = make_schedule(tiles_m, tiles_n, kiters, di->sms * occ, kGroupM, kMinSplitUnits);
+
+  const bool split = sched.dp_tiles < sched.tiles;
+  Workspace* ws = nullptr;
+  st = get_workspace(dev, stream, (size_t)sched.grid,
+                     split ? (size_t)sched.grid * S.BM * S.BN : 0, &ws);
+  if (st != SGEMM_OK) return st;
+  if (++ws->epoch == 0) ws->epoch = 1;
+
+  KernelParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  p.sched = sched;
+  p.ws = ws->partials;
+  p.flags = ws->flags;
+  p.status = ws->status;
+  p.epoch = ws->epoch;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && ((ldc & 3) == 0);
+  p.timeout_ns = g_timeout_ns.load();
+
+  if (cfg.launch(tma, sched.grid, p, &map, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  snprintf(g_last_config, sizeof(g_last_config), "%s b=%s grid=%d dp=%d split=%d kiters=%d",
+           cfg.name, tma ? "tma" : "cp.async", sched.grid, sched.dp_tiles,
+           sched.tiles - sched.dp_tiles, sched.kiters);
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_last_config(char* buf, int len) {
+  if (buf == nullptr || len < 1) return SGEMM_ERR_INVALID_VALUE;
+  snprintf(buf, (size_t)len, "%s", g_last_config);
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_poll_device_status(void* stream_, int* detail) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (detail) *detail = 0;
+  int dev = 0;
+  int st = current_device(&dev);
+  if (st != SGEMM_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  auto it = g_workspaces.find({dev, stream});
+  if (it == g_workspaces.end() || it->second.status == nullptr) return SGEMM_OK;
+  int code = 0;
+  if (cudaMemcpy(&code, it->second.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  if (code != 0) {
+    if (cudaMemset(it->second.status, 0, sizeof(int)) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (detail) *detail = code;
+    return SGEMM_ERR_DEVICE_TIMEOUT;
+  }
+  return SGEMM_OK;
+}
+
+SGEMM_API void sgemm_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int cur = 0;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (auto& kv : g_workspaces) {
+    if (kv.second.block) {
+      cudaSetDevice(kv.first.first);
+      cudaDeviceSynchronize();
+      cudaFree(kv.second.block);
+    }
+  }
+  g_workspaces.clear();
+  if (have_cur) cudaSetDevice(cur);
+  cudaGetLastError();
+}
+
+SGEMM_API int sgemm_config_count(void) { return kNumConfigs; }
+
+SGEMM_API int sgemm_config_info(int id, char* name, int len, int* params) {
+  if (id < 0 || id >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
+  const ConfigEntry& c = *kConfigs[id];
+  if (name != nullptr && len > 0) snprintf(name, (size_t)len, "%s", c.name);
+  if (params != nullptr) {
+    const TileShape& s = c.shape;
+    const int v[11] = {s.BM, s.BN, s.BK, s.WM, s.WN, s.WNITER, s.TM, s.TN, s.NT, s.STAGES, s.MINB};
+    for (int i = 0; i < 11; ++i) params[i] = v[i];
+  }
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_force_config(int id) {
+  if (id < -1 || id >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
+  g_forced.store(id);
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_cfg_check(const int* params, int* derived) {
+  if (params == nullptr) return SGEMM_ERR_INVALID_VALUE;
+  const TileShape s{params[0], params[1], params[2], params[3], params[4], params[5],
+                    params[6], params[7], params[8], params[9], params[10]};
+  const int rule = cfg_check(s);
+  if (rule == 0 && derived != nullptr) {
+    derived[0] = wmiter(s);
+    derived[1] = wsubm(s);
+    derived[2] = wsubn(s);
+    derived[3] = acc_per_thread(s);
+    derived[4] = smem_bytes(s);
+  }
+  return rule;
+}
+
+SGEMM_API int sgemm_schedule_query(int M, int N, int K, int id, int capacity, int* out) {
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
+  if (id < 0 || id >= kNumConfigs || capacity < 1 || out == nullptr)
+    return SGEMM_ERR_INVALID_VALUE;
+  const TileShape& S = kConfigs[id]->shape;
+  const Schedule s = make_schedule((M + S.BM - 1) / S.BM, (N + S.BN - 1) / S.BN,
+                                   (K + S.BK - 1) / S.BK, capacity, kGroupM, kMinSplitUnits);
+  const int v[8] = {s.tiles_m, s.tiles_n, s.kiters, s.grid, s.dp_tiles, s.sk_q, s.sk_r, s.group_m};
+  for (int i = 0; i < 8; ++i) out[i] = v[i];
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_schedule_piece(const int* v, int b, int i, int* out) {
+  if (v == nullptr || out == nullptr) return SGEMM_ERR_INVALID_VALUE;
+  Schedule s{};
+  s.tiles_m = v[0];
+  s.tiles_n = v[1];
+  s.tiles = v[0] * v[1];
+  s.kiters = v[2];
+  s.grid = v[3];
+  s.dp_tiles = v[4];
+  s.sk_q = v[5];
+  s.sk_r = v[6];
+  s.group_m = v[7];
+  s.sk_units = (int64_t)(s.tiles - s.dp_tiles) * s.kiters;
+  if (s.grid < 1 || s.kiters < 1 || s.group_m < 1 || b < 0 || b >= s.grid)
+    return SGEMM_ERR_INVALID_VALUE;
+  const int n = num_pieces(s, b);
+  if (i < 0 || i >= n) return SGEMM_ERR_INVALID_VALUE;
+  const Piece p = get_piece(s, b, i);
+  int tm, tn;
+  tile_coords(s, p.tile, tm, tn);
+  const int o[7] = {p.tile, p.kb, p.ke, tm, tn, num_contributors(s, b, p),
+                    is_partial_piece(s, p) ? 1 : 0};
+  for (int k = 0; k < 7; ++k) out[k] = o[k];
+  return n;
+}
+
+SGEMM_API int sgemm_diag_wait_timeout(long long timeout_ns, void* stream_) {
+  if (timeout_ns < 1000) return SGEMM_ERR_INVALID_VALUE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  int st = current_device(&dev);
+  if (st != SGEMM_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo* di = nullptr;
+  st = device_info(dev, &di);
+  if (st != SGEMM_OK) return st;
+  Workspace* ws = nullptr;
+  st = get_workspace(dev, stream, 1, 0, &ws);
+  if (st != SGEMM_OK) return st;
+  diag_wait_kernel<<<1, 32, 0, stream>>>(ws->status, timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+SGEMM_API long long sgemm_set_wait_timeout_ns(long long ns) {
+  if (ns < 1000) return SGEMM_ERR_INVALID_VALUE;
+  return g_timeout_ns.exchange(ns);
+}

@@ -1,0 +1,505 @@
+// ffma_sgemm.cuh -- the FP32 FFMA SGEMM kernel for sm_103a:
+// C = alpha * A * B + beta * C on row-major matrices with arbitrary M, N, K and
+// leading dimensions.
+//
+// What the pages contribute, and what changed for this part:
+//   * Shared-memory staging of an A and a B tile per k-slice ("Shared Memory
+//     Tiling", kernel listing and "Memory Access Pattern"), here as a ring of
+//     STAGES buffers filled asynchronously and handed over by mbarriers instead
+//     of two __syncthreads per slice.
+//   * A stored transposed, As[k][m], so that a lane's TM values of A for one k
+//     are contiguous and come in with 128-bit shared loads ("Vectorized Memory
+//     Access: 128-bit Loads and Stores", sections "Why As Has To Be Transposed"
+//     and "Mechanics" 1). The transpose still happens on the store side, but
+//     the store is a 4-byte cp.async per element (no registers, no wait) and
+//     the rows are padded so the scattered stores hit 32 distinct banks -- the
+//     page's own "What Could Be Improved" measures 4.2-way conflicts for the
+//     unpadded store.
+//   * B needs no transpose (same page, "Mechanics" 1); it is one TMA box per
+//     k-slice when its pointer and leading dimension allow (16-byte aligned
+//     base, ldb*4 a multiple of 16), else 4-byte cp.async.
+//   * Block / warp / sub-tile / lane decomposition with WMITER x WNITER
+//     interleaved sub-tiles ("Warp Tiling: A Third Level of Tiling", sections
+//     "The Warp Tile Is Not Contiguous Either" and "Mechanics" 1-2). Each lane
+//     keeps WMITER*TM x WNITER*TN accumulators in registers; the default
+//     config uses 16 x 8 = 128 so that one k-step issues 128 FFMA against six
+//     128-bit shared loads (the pages' balance argument in "Shared Memory
+//     Tiling", "What Could Be Improved": at least four FMA per shared load,
+//     counted here per 32-bit word).
+//   * Predicated edges: out-of-range A and B elements are zero-filled by the
+//     copy engines and out-of-range C elements are skipped, so any M, N, K
+//     works (the pages assume divisibility).
+//   * A persistent grid driven by schedule.hpp (whole tiles, then k-split
+//     tiles with a fixed-order fix-up), so every SM gets the same work.
+//   * Epilogue alpha * acc + beta * C with 128-bit read-modify-write where C's
+//     alignment allows; C is not read when beta == 0.
+//
+// Every wait is bounded: a barrier, slot or flag that does not arrive within
+// timeout_ns makes the CTA record a status code, drain its own copies in
+// flight and return, so a fault can never leave the GPU spinning.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "schedule.hpp"
+#include "tile_config.hpp"
+
+namespace sgemm_gb300 {
+
+// Device status codes written to KernelParams::status (first error wins).
+enum DeviceStatus : int {
+  kDevOk = 0,
+  kDevTimeoutFull = 1,    // operand tile never landed
+  kDevTimeoutEmpty = 2,   // a slot was never released by its consumers
+  kDevTimeoutFlag = 3,    // a split partial was never published
+  kDevTimeoutSync = 4,    // a CTA-wide rendezvous did not complete
+};
+
+struct KernelParams {
+  int M, N, K;
+  float alpha, beta;
+  const float* A;
+  long long lda;
+  const float* B;
+  long long ldb;
+  float* C;
+  long long ldc;
+  Schedule sched;
+  float* ws;            // grid * BM * BN floats: one partial tile per CTA
+  uint32_t* flags;      // grid flags: flags[b] == epoch once slot b is written
+  int* status;          // device status word
+  uint32_t epoch;       // value of a flag published by this launch
+  int c_vec;            // C is 16-byte aligned and ldc % 4 == 0
+  long long timeout_ns; // bound on every wait
+};
+
+// Shared-memory layout (from a 1024-byte aligned base):
+//   Bs[STAGES][BK][BN] | As[STAGES][BK][BM + kApad] | fullA[STAGES] |
+//   fullB[STAGES] | empty[STAGES] | sync barrier | abort word
+template <int ST>
+struct BarrierBlock {
+  uint64_t fullA[ST];   // NT cp.async arrivals: this thread's copies landed
+  uint64_t fullB[ST];   // one expect_tx arrival + the TMA transaction bytes
+  uint64_t empty[ST];   // one arrival per warp: the slot may be refilled
+  uint64_t sync;        // CTA-wide rendezvous with a bounded wait
+  int abort;            // set by the first thread that gives up waiting
+};
+
+template <class Cfg>
+constexpr int kernel_smem_bytes() {
+  constexpr TileShape S = Cfg::S;
+  return 1024 + S.STAGES * (a_stage_floats(S) + b_stage_floats(S)) * 4 +
+         (int)sizeof(BarrierBlock<S.STAGES>);
+}
+
+// Bounded wait on an mbarrier phase. Returns false (after recording `code`
+// and raising the CTA's abort word) if the phase does not complete within
+// timeout_ns, or if another thread has already raised the abort word.
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, volatile int* abort_w,
+                                             int* status, int code, long long timeout_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_w) return false;
+    if ((long long)(ptx::global_ns() - t0) > timeout_ns) {
+      *abort_w = 1;
+      atomicCAS(status, 0, code);
+      return false;
+    }
+  }
+}
+
+template <class Cfg, bool kBTma>
+__global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
+    ffma_sgemm_kernel(const __grid_constant__ KernelParams p,
+                      const __grid_constant__ CUtensorMap tmapB) {
+  constexpr TileShape S = Cfg::S;
+  static_assert(cfg_valid(S), "illegal tile configuration");
+  constexpr int BM = S.BM, BN = S.BN, BK = S.BK, NT = S.NT, ST = S.STAGES;
+  constexpr int WM = S.WM, WN = S.WN, TM = S.TM, TN = S.TN, WNITER = S.WNITER;
+  constexpr int WMITER = wmiter(S), WSUBM = wsubm(S), WSUBN = wsubn(S);
+  constexpr int AP = BM + kApad;               // As row pitch (floats)
+  constexpr int A_ST = a_stage_floats(S), B_ST = b_stage_floats(S);
+  constexpr int D = ST - 2;                    // k-slices loaded ahead
+  constexpr int LANES_N = WSUBN / TN;          // lanes along n in a sub-tile
+  constexpr int RM = WMITER * TM, RN = WNITER * TN;  // a lane's rows / cols
+  constexpr int A_ROWS = NT / kAloadK;         // rows of A per load pass
+  constexpr int A_MG = BM / A_ROWS, A_KG = BK / kAloadK;
+  constexpr int B_PASSES = (BK * BN) / NT;
+  constexpr int WARPS_N = BN / WN;
+  constexpr uint32_t FULL = 0xffffffffu;
+
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  float* Bs = reinterpret_cast<float*>(base);
+  float* As = Bs + ST * B_ST;
+  BarrierBlock<ST>* bb = reinterpret_cast<BarrierBlock<ST>*>(As + ST * A_ST);
+  volatile int* abort_w = &bb->abort;
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int b = blockIdx.x;
+  const Schedule& sc = p.sched;
+
+  if (tid == 0) {
+    for (int s = 0; s < ST; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&bb->fullA[s]), NT);
+      ptx::mbar_init(ptx::smem_addr(&bb->fullB[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bb->empty[s]), NT / 32);
+    }
+    ptx::mbar_init(ptx::smem_addr(&bb->sync), NT);
+    bb->abort = 0;
+    ptx::mbar_fence_init();
+    if (kBTma) ptx::tma_prefetch_desc(&tmapB);
+  }
+  __syncthreads();
+
+  const int npieces = num_pieces(sc, b);
+  const int nsteps = (int)total_steps(sc, b);
+
+  // ---- lane geometry --------------------------------------------------------
+  const int warp_m = warp / WARPS_N, warp_n = warp % WARPS_N;
+  const int lr = lane / LANES_N, lc = lane % LANES_N;
+  // fragment read offsets inside one stage (floats)
+  const int a_frag_off = warp_m * WM + lr * TM;
+  const int b_frag_off = warp_n * WN + lc * TN;
+  // A loader: this thread copies k = kg*8 + a_k of rows mg*A_ROWS + a_m
+  const int a_k = tid % kAloadK, a_m = tid / kAloadK;
+  const uint32_t a_dst0 = (uint32_t)((a_k * AP + a_m) * 4);
+
+  const float* __restrict__ Ag = p.A;
+  const float* __restrict__ Bg = p.B;
+  const int M = p.M, N = p.N, K = p.K;
+  const long long lda = p.lda, ldb = p.ldb;
+
+  const uint32_t As_addr = ptx::smem_addr(As);
+  const uint32_t Bs_addr = ptx::smem_addr(Bs);
+
+  // ---- load cursor: which (tile, k-slice) the next issued step is ---------
+  int l_piece = 0, l_k = 0, l_ke = 0, l_m0 = 0, l_n0 = 0;
+  if (npieces > 0) {
+    const Piece lp = get_piece(sc, b, 0);
+    int tm, tn;
+    tile_coords(sc, lp.tile, tm, tn);
+    l_k = lp.kb;
+    l_ke = lp.ke;
+    l_m0 = tm * BM;
+    l_n0 = tn * BN;
+  }
+  int issued = 0;
+
+  // Issue the copies of step `step` (k-slice l_k of the cursor's tile) into
+  // its ring slot, then advance the cursor. Returns false on abort.
+  auto issue_next = [&]() -> bool {
+    const int slot = issued % ST;
+    if (issued >= ST) {
+      const uint32_t par = (uint32_t)((issued / ST) & 1) ^ 1u;
+      const bool ok = bounded_wait(ptx::smem_addr(&bb->empty[slot]), par, abort_w, p.status,
+                                   kDevTimeoutEmpty, p.timeout_ns);
+      if (!__all_sync(FULL, ok)) return false;
+    }
+    const int k0 = l_k * BK;
+    // A: transposed on store, As[k][m] <- A[m0 + m][k0 + k], zero outside
+    const uint32_t a_slot = As_addr + (uint32_t)(slot * A_ST * 4) + a_dst0;
+#pragma unroll
+    for (int mg = 0; mg < A_MG; ++mg) {
+      const int row = l_m0 + mg * A_ROWS + a_m;
+      const bool row_ok = row < M;
+      const float* src_row = Ag + (row_ok ? (long long)row * lda : 0);
+#pragma unroll
+      for (int kg = 0; kg < A_KG; ++kg) {
+        const int k = k0 + kg * kAloadK + a_k;
+        const bool ok = row_ok && (k < K);
+        ptx::cp_async_4(a_slot + (uint32_t)((kg * kAloadK * AP + mg * A_ROWS) * 4),
+                        ok ? (const void*)(src_row + k) : (const void*)Ag, ok ? 4u : 0u);
+      }
+    }
+    if (!kBTma) {
+      // B without TMA: Bs[k][n] <- B[k0 + k][n0 + n], zero outside
+      const uint32_t b_slot = Bs_addr + (uint32_t)(slot * B_ST * 4);
+#pragma unroll
+      for (int ps = 0; ps < B_PASSES; ++ps) {
+        const int e = ps * NT + tid;
+        const int kk = e / BN, nn = e % BN;
+        const int k = k0 + kk, n = l_n0 + nn;
+        const bool ok = (k < K) && (n < N);
+        ptx::cp_async_4(b_slot + (uint32_t)(e * 4),
+                        ok ? (const void*)(Bg + (long long)k * ldb + n) : (const void*)Bg,
+                        ok ? 4u : 0u);
+      }
+    }
+    ptx::cp_async_arrive_noinc(ptx::smem_addr(&bb->fullA[slot]));
+    if (kBTma && tid == 0) {
+      const uint32_t fb = ptx::smem_addr(&bb->fullB[slot]);
+      ptx::mbar_arrive_expect_tx(fb, (uint32_t)(BK * BN * 4));
+      ptx::tma_load_2d(Bs_addr + (uint32_t)(slot * B_ST * 4), &tmapB, l_n0, k0, fb);
+    }
+    ++issued;
+    if (++l_k == l_ke) {
+      if (++l_piece < npieces) {
+        const Piece lp = get_piece(sc, b, l_piece);
+        int tm, tn;
+        tile_coords(sc, lp.tile, tm, tn);
+        l_k = lp.kb;
+        l_ke = lp.ke;
+        l_m0 = tm * BM;
+        l_n0 = tn * BN;
+      }
+    }
+    return true;
+  };
+
+  float acc[RM][RN];
+#pragma unroll
+  for (int i = 0; i < RM; ++i)
+#pragma unroll
+    for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
+
+  uint32_t sync_phase = 0;
+  // CTA-wide rendezvous with a bounded wait (a plain __syncthreads could not
+  // be abandoned if another warp has given up).
+  auto cta_sync = [&]() -> bool {
+    ptx::mbar_arrive(ptx::smem_addr(&bb->sync));
+    const bool ok = bounded_wait(ptx::smem_addr(&bb->sync), sync_phase, abort_w, p.status,
+                                 kDevTimeoutSync, p.timeout_ns);
+    sync_phase ^= 1u;
+    return __all_sync(FULL, ok);
+  };
+
+  bool aborted = false;
+  for (int s = 0; s < D && issued < nsteps; ++s) {
+    if (!issue_next()) {
+      aborted = true;
+      break;
+    }
+  }
+
+  int c_piece = 0, c_k = 0;
+  Piece cpc{0, 0, 0};
+  if (npieces > 0) {
+    cpc = get_piece(sc, b, 0);
+    c_k = cpc.kb;
+  }
+
+  for (int step = 0; step < nsteps && !aborted; ++step) {
+    if (issued < nsteps) {
+      if (!issue_next()) {
+        aborted = true;
+        break;
+      }
+    }
+    const int slot = step % ST;
+    const uint32_t par = (uint32_t)((step / ST) & 1);
+    {
+      bool ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
+                             kDevTimeoutFull, p.timeout_ns);
+      if (kBTma && ok)
+        ok = bounded_wait(ptx::smem_addr(&bb->fullB[slot]), par, abort_w, p.status,
+                          kDevTimeoutFull, p.timeout_ns);
+      if (!__all_sync(FULL, ok)) {
+        aborted = true;
+        break;
+      }
+    }
+
+    // ---- BK k-steps of outer-product FFMA on this slot -----------------------
+    const float* a_s = As + slot * A_ST + a_frag_off;
+    const float* b_s = Bs + slot * B_ST + b_frag_off;
+    float af[2][RM], bfr[2][RN];
+#pragma unroll
+    for (int wm = 0; wm < WMITER; ++wm)
+#pragma unroll
+      for (int q = 0; q < TM / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(a_s + wm * WSUBM + q * 4);
+        af[0][wm * TM + q * 4 + 0] = v.x;
+        af[0][wm * TM + q * 4 + 1] = v.y;
+        af[0][wm * TM + q * 4 + 2] = v.z;
+        af[0][wm * TM + q * 4 + 3] = v.w;
+      }
+#pragma unroll
+    for (int wn = 0; wn < WNITER; ++wn)
+#pragma unroll
+      for (int q = 0; q < TN / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(b_s + wn * WSUBN + q * 4);
+        bfr[0][wn * TN + q * 4 + 0] = v.x;
+        bfr[0][wn * TN + q * 4 + 1] = v.y;
+        bfr[0][wn * TN + q * 4 + 2] = v.z;
+        bfr[0][wn * TN + q * 4 + 3] = v.w;
+      }
+#pragma unroll
+    for (int k = 0; k < BK; ++k) {
+      const int cur = k & 1, nxt = cur ^ 1;
+      if (k + 1 < BK) {
+#pragma unroll
+        for (int wm = 0; wm < WMITER; ++wm)
+#pragma unroll
+          for (int q = 0; q < TM / 4; ++q) {
+            const float4 v =
+                *reinterpret_cast<const float4*>(a_s + (k + 1) * AP + wm * WSUBM + q * 4);
+            af[nxt][wm * TM + q * 4 + 0] = v.x;
+            af[nxt][wm * TM + q * 4 + 1] = v.y;
+            af[nxt][wm * TM + q * 4 + 2] = v.z;
+            af[nxt][wm * TM + q * 4 + 3] = v.w;
+          }
+#pragma unroll
+        for (int wn = 0; wn < WNITER; ++wn)
+#pragma unroll
+          for (int q = 0; q < TN / 4; ++q) {
+            const float4 v =
+                *reinterpret_cast<const float4*>(b_s + (k + 1) * BN + wn * WSUBN + q * 4);
+            bfr[nxt][wn * TN + q * 4 + 0] = v.x;
+            bfr[nxt][wn * TN + q * 4 + 1] = v.y;
+            bfr[nxt][wn * TN + q * 4 + 2] = v.z;
+            bfr[nxt][wn * TN + q * 4 + 3] = v.w;
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j = 0; j < RN; ++j) acc[i][j] = fmaf(af[cur][i], bfr[cur][j], acc[i][j]);
+    }
+
+    // release the slot: one arrival per warp once all its lanes are done
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bb->empty[slot]));
+
+    if (++c_k < cpc.ke) continue;
+
+    // ---- the current piece is complete: publish a partial or write C --------
+    float* ws_tile = p.ws + (long long)b * (BM * BN);
+    if (is_partial_piece(sc, cpc)) {
+      float4* dst = reinterpret_cast<float4*>(ws_tile);
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j4 = 0; j4 < RN / 4; ++j4)
+          __stcg(dst + (i * (RN / 4) + j4) * NT + tid,
+                 make_float4(acc[i][j4 * 4 + 0], acc[i][j4 * 4 + 1], acc[i][j4 * 4 + 2],
+                             acc[i][j4 * 4 + 3]));
+      if (!cta_sync()) {
+        aborted = true;
+        break;
+      }
+      if (tid == 0) {
+        __threadfence();
+        ptx::st_release(p.flags + b, p.epoch);
+      }
+    } else {
+      const int nc = num_contributors(sc, b, cpc);
+      if (nc > 0) {
+        if (tid == 0) {
+          for (int c = 1; c <= nc; ++c) {
+            const uint32_t* f = p.flags + b + c;
+            if (ptx::ld_acquire(f) == p.epoch) continue;
+            const uint64_t t0 = ptx::global_ns();
+            while (ptx::ld_acquire(f) != p.epoch) {
+              if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) {
+                *abort_w = 1;
+                atomicCAS(p.status, 0, (int)kDevTimeoutFlag);
+                break;
+              }
+              __nanosleep(200);
+            }
+            if (*abort_w) break;
+          }
+        }
+        if (!cta_sync() || *abort_w) {
+          aborted = true;
+          break;
+        }
+        // add the partials of CTAs b+1 .. b+nc, in that order
+        for (int c = 1; c <= nc; ++c) {
+          const float4* src = reinterpret_cast<const float4*>(ws_tile + (long long)c * (BM * BN));
+#pragma unroll
+          for (int i = 0; i < RM; ++i)
+#pragma unroll
+            for (int j4 = 0; j4 < RN / 4; ++j4) {
+              const float4 v = __ldcg(src + (i * (RN / 4) + j4) * NT + tid);
+              acc[i][j4 * 4 + 0] += v.x;
+              acc[i][j4 * 4 + 1] += v.y;
+              acc[i][j4 * 4 + 2] += v.z;
+              acc[i][j4 * 4 + 3] += v.w;
+            }
+        }
+      }
+      // epilogue: C = alpha * acc + beta * C for this lane's RM x RN patch
+      int tm, tn;
+      tile_coords(sc, cpc.tile, tm, tn);
+      const int row0 = tm * BM + a_frag_off;
+      const int col0 = tn * BN + b_frag_off;
+      const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+      for (int wm = 0; wm < WMITER; ++wm)
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+          const int row = row0 + wm * WSUBM + i;
+          if (row >= M) continue;
+          float* crow = p.C + (long long)row * p.ldc;
+          const float* a = acc[wm * TM + i];
+#pragma unroll
+          for (int wn = 0; wn < WNITER; ++wn)
+#pragma unroll
+            for (int q = 0; q < TN / 4; ++q) {
+              const int col = col0 + wn * WSUBN + q * 4;
+              const float* r = a + wn * TN + q * 4;
+              if (p.c_vec && col + 3 < N) {
+                float4 v;
+                if (beta != 0.f) {
+                  const float4 old = *reinterpret_cast<const float4*>(crow + col);
+                  v.x = fmaf(alpha, r[0], beta * old.x);
+                  v.y = fmaf(alpha, r[1], beta * old.y);
+                  v.z = fmaf(alpha, r[2], beta * old.z);
+                  v.w = fmaf(alpha, r[3], beta * old.w);
+                } else {
+                  v = make_float4(alpha * r[0], alpha * r[1], alpha * r[2], alpha * r[3]);
+                }
+                *reinterpret_cast<float4*>(crow + col) = v;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  if (col + e < N) {
+                    crow[col + e] = beta != 0.f ? fmaf(alpha, r[e], beta * crow[col + e])
+                                                : alpha * r[e];
+                  }
+                }
+              }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RM; ++i)
+#pragma unroll
+      for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
+    if (++c_piece < npieces) {
+      cpc = get_piece(sc, b, c_piece);
+      c_k = cpc.kb;
+    }
+  }
+
+  if (aborted) {
+    // Drain this thread's copies; the TMA issuer also waits (bounded) for
+    // the B tiles it issued and nobody consumed, so nothing lands in shared
+    // memory after the CTA is gone.
+    ptx::cp_async_wait_all();
+    if (kBTma && tid == 0) {
+      const uint64_t t0 = ptx::global_ns();
+      for (int s = issued - 1; s >= 0 && s >= issued - ST; --s) {
+        const uint32_t fb = ptx::smem_addr(&bb->fullB[s % ST]);
+        const uint32_t par = (uint32_t)((s / ST) & 1);
+        while (!ptx::mbar_try_wait(fb, par)) {
+          if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+        }
+      }
+    }
+    __nanosleep(20000);
+  }
+}
+
+}  // namespace sgemm_gb300

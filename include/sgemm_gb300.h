@@ -1,0 +1,147 @@
+/*
+ * sgemm_gb300.h -- C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * The operation is the one every kernel on the pages computes:
+ *   C = alpha * A * B + beta * C
+ * on row-major FP32 matrices ("Shared Memory Tiling", kernel listing, final
+ * store alpha * acc + beta * C; "Warp Tiling: A Third Level of Tiling",
+ * section "The Kernel", epilogue; "Vectorized Memory Access: 128-bit Loads and
+ * Stores", section "The Kernel", epilogue). The pages' kernels take
+ * (M, N, K, alpha, A, B, beta, C) with implicit leading dimensions lda = K,
+ * ldb = ldc = N; this interface adds explicit leading dimensions and a stream.
+ *
+ * Layout (row-major): A(i,k) = A[i*lda + k] for i < M, k < K;
+ *                     B(k,j) = B[k*ldb + j] for k < K, j < N;
+ *                     C(i,j) = C[i*ldc + j] for i < M, j < N.
+ * Elements outside those ranges (padding between rows) are never read or
+ * written.
+ *
+ * Ownership: all matrix pointers are DEVICE pointers owned by the caller. The
+ * library owns only a small per-(device, stream) workspace (split-K partial
+ * tiles, their flags and a device status word), allocated on first use and
+ * released by sgemm_shutdown(). No call here takes a torch type.
+ *
+ * Errors: every function returns an sgemm_status. Argument errors are found on
+ * the host before anything is launched, and leave C untouched. Launch errors
+ * are returned synchronously. A kernel that gives up on a bounded wait (a
+ * copy, slot or partial that never arrived within the wait limit) records a
+ * device status that sgemm_poll_device_status() reports.
+ *
+ * Threading: calls are asynchronous with respect to the host and ordered on
+ * `stream`; the workspace is per (device, stream), so concurrent calls on
+ * different streams do not share it. Host-side state is guarded by a mutex.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SGEMM_OK = 0,
+  SGEMM_ERR_INVALID_DIM = -1,       /* M, N or K negative                        */
+  SGEMM_ERR_INVALID_LD = -2,        /* lda < max(1,K), ldb < max(1,N), ldc < max(1,N) */
+  SGEMM_ERR_NULL_PTR = -3,          /* a matrix that must be accessed is NULL     */
+  SGEMM_ERR_UNSUPPORTED_DEVICE = -4,/* current device is not sm_103               */
+  SGEMM_ERR_LAUNCH = -5,            /* CUDA runtime error while launching         */
+  SGEMM_ERR_DEVICE_TIMEOUT = -6,    /* a kernel gave up on a bounded wait         */
+  SGEMM_ERR_ALLOC = -7,             /* workspace allocation failed                */
+  SGEMM_ERR_MISALIGNED = -8,        /* a matrix pointer is not 4-byte aligned     */
+  SGEMM_ERR_INVALID_VALUE = -9      /* other invalid argument (config id, buffer) */
+} sgemm_status;
+
+/*
+ * C = alpha * A * B + beta * C (FP32, FFMA path).
+ *
+ * M, N, K >= 0. lda >= max(1, K), ldb >= max(1, N), ldc >= max(1, N).
+ * Quick returns: M == 0 or N == 0 does nothing. K == 0 or alpha == 0 scales
+ * C by beta without reading A or B. beta == 0 never reads C, so C may hold
+ * NaN or garbage. A and B may have any 4-byte alignment (the 128-bit and TMA
+ * paths are used only when alignment allows). C must not overlap A or B.
+ * stream: a cudaStream_t (NULL = legacy default stream).
+ */
+int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+          float beta, float* C, int ldc, void* stream);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* sgemm_status_string(int status);
+
+/*
+ * Name of the tile configuration and schedule the calling thread's last
+ * sgemm() used, copied into buf (at most len bytes, NUL-terminated).
+ * Returns SGEMM_OK, or SGEMM_ERR_INVALID_VALUE if buf is NULL or len < 1.
+ */
+int sgemm_last_config(char* buf, int len);
+
+/*
+ * Waits for `stream`, then reports and clears the device status word of this
+ * (device, stream) workspace: SGEMM_OK, or SGEMM_ERR_DEVICE_TIMEOUT if a
+ * kernel gave up on a bounded wait since the last poll. *detail (if not NULL)
+ * receives the device-side code (1 = operand tile, 2 = slot release, 3 =
+ * split partial, 4 = CTA rendezvous). SGEMM_ERR_LAUNCH if synchronising fails.
+ */
+int sgemm_poll_device_status(void* stream, int* detail);
+
+/* Frees every workspace the library allocated (after synchronising the
+ * device). Later calls allocate again. */
+void sgemm_shutdown(void);
+
+/*
+ * Tile configurations compiled into the library. sgemm_config_count() gives
+ * their number; sgemm_config_info() fills name (len bytes) and the tile
+ * parameters of configuration `id` as
+ * {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB} in params[11].
+ */
+int sgemm_config_count(void);
+int sgemm_config_info(int id, char* name, int len, int* params);
+
+/*
+ * Forces every later sgemm() on this process to use configuration `id`
+ * (-1 restores the automatic per-shape choice). For tuning and tests.
+ */
+int sgemm_force_config(int id);
+
+/*
+ * The legality checker of the tile configurations, evaluated on the host:
+ * 0 if the tuple is legal for the FFMA kernel, else the number of the first
+ * rule it breaks. params = {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES,
+ * MINB}. derived (if not NULL) receives {WMITER, WSUBM, WSUBN, accumulators
+ * per thread, shared bytes per CTA} when the tuple is legal.
+ */
+int sgemm_cfg_check(const int* params, int* derived);
+
+/*
+ * The persistent schedule sgemm() would use for an M x N x K problem with
+ * configuration `id` on `capacity` resident CTAs (host arithmetic only, no
+ * device needed). out = {tiles_m, tiles_n, kiters, grid, dp_tiles, sk_q,
+ * sk_r, group_m}. Returns SGEMM_OK or an argument error.
+ */
+int sgemm_schedule_query(int M, int N, int K, int id, int capacity, int* out);
+
+/*
+ * Piece `i` of CTA `b` under the schedule {tiles_m, tiles_n, kiters, grid,
+ * dp_tiles, sk_q, sk_r, group_m} (as returned above): out = {tile, kb, ke,
+ * tile_m, tile_n, contributors, is_partial}. Returns the number of pieces of
+ * CTA b, or a negative status. Host arithmetic only.
+ */
+int sgemm_schedule_piece(const int* sched, int b, int i, int* out);
+
+/*
+ * Diagnostic: launches one CTA that waits on a shared-memory barrier nothing
+ * ever arrives on, with a limit of timeout_ns, through the same bounded wait
+ * the GEMM kernels use. The wait must run out and record device code 1; read
+ * it with sgemm_poll_device_status(). Nothing faults and nothing hangs.
+ */
+int sgemm_diag_wait_timeout(long long timeout_ns, void* stream);
+
+/* Upper bound, in nanoseconds, of every wait inside the kernels (default
+ * 4e9). Values < 1000 are rejected. Returns the previous value or a negative
+ * status. */
+long long sgemm_set_wait_timeout_ns(long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */
