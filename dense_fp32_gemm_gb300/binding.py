@@ -26,7 +26,7 @@ SGEMM_ERR_ALLOC = -7
 SGEMM_ERR_MISALIGNED = -8
 SGEMM_ERR_INVALID_VALUE = -9
 
-PARAM_NAMES = ("BM", "BN", "BK", "WM", "WN", "WNITER", "TM", "TN", "NT", "STAGES", "MINB")
+PARAM_NAMES = ("BM", "BN", "BK", "WM", "WN", "WNITER", "TM", "TN", "NT", "STAGES", "MINB", "KU", "ORDER")
 
 
 class SgemmError(RuntimeError):
@@ -117,7 +117,7 @@ def sgemm_config_count() -> int:
 
 def sgemm_config_info(cid: int):
     name = ctypes.create_string_buffer(128)
-    params = _ints(11)
+    params = _ints(13)
     st = lib().sgemm_config_info(cid, name, 128, params)
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm_config_info")
@@ -133,7 +133,7 @@ def sgemm_cfg_check(params):
     acc_per_thread, smem_bytes} for a legal tuple."""
     if isinstance(params, dict):
         params = [params[k] for k in PARAM_NAMES]
-    p = _ints(11, params)
+    p = _ints(13, params)
     d = _ints(5)
     rule = lib().sgemm_cfg_check(p, d)
     derived = dict(zip(("WMITER", "WSUBM", "WSUBN", "acc", "smem_bytes"), list(d))) if rule == 0 else None

@@ -26,9 +26,14 @@ namespace sgemm_gb300 {
 namespace {
 
 // ---- configuration registry -------------------------------------------------
-const ConfigEntry* const kConfigs[] = {&kEntryWide, &kEntryTall, &kEntrySquare, &kEntryPages};
+#define SGEMM_GB300_ENTRY_PTR(NAME, ...) &kEntry##NAME,
+const ConfigEntry* const kConfigs[] = {SGEMM_GB300_CONFIGS(SGEMM_GB300_ENTRY_PTR)};
+#undef SGEMM_GB300_ENTRY_PTR
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
-enum : int { kIdWide = 0, kIdTall = 1, kIdSquare = 2, kIdPages = 3 };
+#define SGEMM_GB300_ENTRY_ID(NAME, ...) kId##NAME,
+enum ConfigId : int { SGEMM_GB300_CONFIGS(SGEMM_GB300_ENTRY_ID) kIdCount };
+#undef SGEMM_GB300_ENTRY_ID
+static_assert(kIdCount == kNumConfigs, "config ids");
 
 // Raster group height (tiles) and the fewest k-slices worth splitting off.
 constexpr int kGroupM = 8;
@@ -142,10 +147,9 @@ int get_workspace(int dev, cudaStream_t stream, size_t flags, size_t partial_flo
 // Automatic choice of tile configuration by shape class.
 int choose_config(int M, int N, int K, int sms) {
   (void)K;
-  if (N <= 96) return kIdTall;
-  const long long wide_tiles = (long long)((M + 127) / 128) * ((N + 255) / 256);
-  if (wide_tiles >= sms) return kIdWide;
-  return kIdSquare;
+  (void)sms;
+  if (N <= 96) return kIdTallBk24;
+  return kIdWideBk32F2;
 }
 
 __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {
@@ -353,8 +357,9 @@ SGEMM_API int sgemm_config_info(int id, char* name, int len, int* params) {
   if (name != nullptr && len > 0) snprintf(name, (size_t)len, "%s", c.name);
   if (params != nullptr) {
     const TileShape& s = c.shape;
-    const int v[11] = {s.BM, s.BN, s.BK, s.WM, s.WN, s.WNITER, s.TM, s.TN, s.NT, s.STAGES, s.MINB};
-    for (int i = 0; i < 11; ++i) params[i] = v[i];
+    const int v[13] = {s.BM, s.BN, s.BK, s.WM, s.WN, s.WNITER, s.TM, s.TN, s.NT, s.STAGES, s.MINB,
+                       s.KU, s.ORDER};
+    for (int i = 0; i < 13; ++i) params[i] = v[i];
   }
   return SGEMM_OK;
 }
@@ -367,8 +372,8 @@ SGEMM_API int sgemm_force_config(int id) {
 
 SGEMM_API int sgemm_cfg_check(const int* params, int* derived) {
   if (params == nullptr) return SGEMM_ERR_INVALID_VALUE;
-  const TileShape s{params[0], params[1], params[2], params[3], params[4], params[5],
-                    params[6], params[7], params[8], params[9], params[10]};
+  const TileShape s{params[0], params[1], params[2], params[3], params[4],  params[5],
+                    params[6], params[7], params[8], params[9], params[10], params[11], params[12]};
   const int rule = cfg_check(s);
   if (rule == 0 && derived != nullptr) {
     derived[0] = wmiter(s);

@@ -16,29 +16,43 @@ namespace sgemm_gb300 {
 
 struct KernelParams;
 
-// 128 x 256 CTA tile, 8 warps of 64 x 64, 16 x 8 accumulators per lane:
-// the large-problem shape (B arrives by TMA, so a wide BN costs no loader
-// instructions).
-struct CfgWide {
-  static constexpr TileShape S{128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1};
-  static constexpr const char* name = "wide128x256x16_w64x64_t16x8_s4";
-};
-// 256 x 64 CTA tile, 4 warps of 64 x 64: for N <= 64 (skinny outputs).
-struct CfgTall {
-  static constexpr TileShape S{256, 64, 16, 64, 64, 2, 4, 4, 128, 4, 2};
-  static constexpr const char* name = "tall256x64x16_w64x64_t16x8_s4";
-};
-// 128 x 128 CTA tile, 4 warps of 64 x 64, two CTAs per SM.
-struct CfgSquare {
-  static constexpr TileShape S{128, 128, 16, 64, 64, 2, 4, 4, 128, 4, 2};
-  static constexpr const char* name = "square128x128x16_w64x64_t16x8_s4";
-};
-// The pages' sweep winner (128 x 64 x 16, warp 64 x 32, WNITER 2, 4 x 4
-// patches, 128 threads) on this kernel's pipeline: 8 x 8 accumulators.
-struct CfgPages {
-  static constexpr TileShape S{128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 4};
-  static constexpr const char* name = "pages128x64x16_w64x32_t8x8_s3";
-};
+// Every configuration compiled into the library, in registry order:
+//   X(Name, BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB, KU, ORDER)
+// wide:    128 x 256 CTA tile, 8 warps of 64 x 64, 16 x 8 accumulators per lane
+//          (B arrives by TMA, so a wide BN costs no loader instructions);
+// tall:    256 x 64, 4 warps of 64 x 64, for N <= 64;
+// square:  128 x 128, 4 warps of 64 x 64, two CTAs per SM;
+// pages:   the pages' sweep winner (128 x 64 x 16, warp 64 x 32, WNITER 2,
+//          4 x 4 patches, 128 threads) on this kernel's pipeline;
+// the rest vary the k-slice depth (BK), the unrolled chunk (KU) and the
+// pipeline depth of the wide shape, for the tuner.
+#define SGEMM_GB300_CONFIGS(X)                                     \
+  X(Wide, 128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1, 4, 0)          \
+  X(Tall, 256, 64, 16, 64, 64, 2, 4, 4, 128, 4, 2, 4, 0)           \
+  X(Square, 128, 128, 16, 64, 64, 2, 4, 4, 128, 4, 2, 4, 0)        \
+  X(Pages, 128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 3, 4, 0)          \
+  X(WideKu8, 128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1, 8, 0)       \
+  X(WideBk32, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 4, 0)      \
+  X(WideBk32Ku8, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 8, 0)   \
+  X(WideBk32Ku8Zz, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 8, 1) \
+  X(WideBk48Ku8, 128, 256, 48, 64, 64, 2, 4, 4, 256, 3, 1, 8, 0)   \
+  X(SquareBk32, 128, 128, 32, 64, 64, 2, 4, 4, 128, 3, 2, 8, 0)    \
+  X(TallBk24, 256, 64, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 0)       \
+  X(WideBk32F2, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 8, 2)    \
+  X(WideBk48F2, 128, 256, 48, 64, 64, 2, 4, 4, 256, 3, 1, 8, 2)    \
+  X(WideBk16F2, 128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1, 8, 2)    \
+  X(SquareBk32F2, 128, 128, 32, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)  \
+  X(TallBk24F2, 256, 64, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)
+
+#define SGEMM_GB300_CFG_STRUCT(NAME, BM, BN, BK, WM, WN, WNI, TM, TN, NT, ST, MINB, KU, OR)     \
+  struct Cfg##NAME {                                                                            \
+    static constexpr TileShape S{BM, BN, BK, WM, WN, WNI, TM, TN, NT, ST, MINB, KU, OR};        \
+    static constexpr const char* name = #NAME "_" #BM "x" #BN "x" #BK "_w" #WM "x" #WN          \
+                                        "_n" #WNI "_p" #TM "x" #TN "_t" #NT "_s" #ST "_u" #KU   \
+                                        "_o" #OR;                                               \
+  };
+SGEMM_GB300_CONFIGS(SGEMM_GB300_CFG_STRUCT)
+#undef SGEMM_GB300_CFG_STRUCT
 
 using LaunchFn = cudaError_t (*)(bool tma, int grid, const KernelParams& p, const CUtensorMap* map,
                                  cudaStream_t stream);
@@ -54,10 +68,9 @@ struct ConfigEntry {
   LaunchFn launch;
 };
 
-// Defined in the cfg_*.cu translation units.
-extern const ConfigEntry kEntryWide;
-extern const ConfigEntry kEntryTall;
-extern const ConfigEntry kEntrySquare;
-extern const ConfigEntry kEntryPages;
+// Defined in the cfg_*.cu translation units, one per configuration.
+#define SGEMM_GB300_DECLARE_ENTRY(NAME, ...) extern const ConfigEntry kEntry##NAME;
+SGEMM_GB300_CONFIGS(SGEMM_GB300_DECLARE_ENTRY)
+#undef SGEMM_GB300_DECLARE_ENTRY
 
 }  // namespace sgemm_gb300

@@ -42,6 +42,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "ptx.cuh"
 #include "schedule.hpp"
 #include "tile_config.hpp"
@@ -90,8 +92,8 @@ struct BarrierBlock {
 template <class Cfg>
 constexpr int kernel_smem_bytes() {
   constexpr TileShape S = Cfg::S;
-  return 1024 + S.STAGES * (a_stage_floats(S) + b_stage_floats(S)) * 4 +
-         (int)sizeof(BarrierBlock<S.STAGES>);
+  static_assert(sizeof(BarrierBlock<S.STAGES>) <= S.STAGES * 3 * 8 + 16, "barrier block size");
+  return smem_bytes(S);
 }
 
 // Bounded wait on an mbarrier phase. Returns false (after recording `code`
@@ -114,13 +116,31 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, vola
   }
 }
 
+// Interior A copies of one row group: for each k-group KG, one 4-byte copy
+// with both offsets compile-time (destination: KG*8 rows of As plus the
+// group's MG*A_ROWS columns; source: KG*8 floats along the row).
+template <int AP, int A_ROWS, int MG, int... KG>
+__device__ __forceinline__ void issue_a_group(uint32_t dst, const float* src,
+                                              std::integer_sequence<int, KG...>) {
+  (ptx::cp_async_4_imm<(KG * kAloadK * AP + MG * A_ROWS) * 4, KG * kAloadK * 4>(dst, src), ...);
+}
+
+// All interior A copies of one k-slice: row group MG starts MG*stride floats
+// after the first.
+template <int AP, int A_ROWS, int A_KG, int... MG>
+__device__ __forceinline__ void issue_a_tile(uint32_t dst, const float* src, long long stride,
+                                             std::integer_sequence<int, MG...>) {
+  (issue_a_group<AP, A_ROWS, MG>(dst, src + MG * stride, std::make_integer_sequence<int, A_KG>{}),
+   ...);
+}
+
 template <class Cfg, bool kBTma>
 __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     ffma_sgemm_kernel(const __grid_constant__ KernelParams p,
                       const __grid_constant__ CUtensorMap tmapB) {
   constexpr TileShape S = Cfg::S;
   static_assert(cfg_valid(S), "illegal tile configuration");
-  constexpr int BM = S.BM, BN = S.BN, BK = S.BK, NT = S.NT, ST = S.STAGES;
+  constexpr int BM = S.BM, BN = S.BN, BK = S.BK, NT = S.NT, ST = S.STAGES, KU = S.KU;
   constexpr int WM = S.WM, WN = S.WN, TM = S.TM, TN = S.TN, WNITER = S.WNITER;
   constexpr int WMITER = wmiter(S), WSUBM = wsubm(S), WSUBN = wsubn(S);
   constexpr int AP = BM + kApad;               // As row pitch (floats)
@@ -178,25 +198,31 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   const float* __restrict__ Bg = p.B;
   const int M = p.M, N = p.N, K = p.K;
   const long long lda = p.lda, ldb = p.ldb;
+  const long long a_group_stride = (long long)A_ROWS * lda;  // floats between row groups
 
   const uint32_t As_addr = ptx::smem_addr(As);
   const uint32_t Bs_addr = ptx::smem_addr(Bs);
 
   // ---- load cursor: which (tile, k-slice) the next issued step is ---------
   int l_piece = 0, l_k = 0, l_ke = 0, l_m0 = 0, l_n0 = 0;
-  if (npieces > 0) {
-    const Piece lp = get_piece(sc, b, 0);
+  bool l_m_inside = false;            // all BM rows of the tile are < M
+  const float* l_arow = Ag;           // A + (m0 + a_m) * lda
+  auto set_load_piece = [&](int i) {
+    const Piece lp = get_piece(sc, b, i);
     int tm, tn;
     tile_coords(sc, lp.tile, tm, tn);
     l_k = lp.kb;
     l_ke = lp.ke;
     l_m0 = tm * BM;
     l_n0 = tn * BN;
-  }
+    l_m_inside = l_m0 + BM <= M;
+    l_arow = Ag + (l_m_inside ? (long long)(l_m0 + a_m) * lda : 0);
+  };
+  if (npieces > 0) set_load_piece(0);
   int issued = 0;
 
-  // Issue the copies of step `step` (k-slice l_k of the cursor's tile) into
-  // its ring slot, then advance the cursor. Returns false on abort.
+  // Issue the copies of the next step into its ring slot, then advance the
+  // cursor. Returns false on abort.
   auto issue_next = [&]() -> bool {
     const int slot = issued % ST;
     if (issued >= ST) {
@@ -208,17 +234,23 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     const int k0 = l_k * BK;
     // A: transposed on store, As[k][m] <- A[m0 + m][k0 + k], zero outside
     const uint32_t a_slot = As_addr + (uint32_t)(slot * A_ST * 4) + a_dst0;
+    if (l_m_inside && k0 + BK <= K) {
+      // interior slice: no predicates, immediate offsets
+      issue_a_tile<AP, A_ROWS, A_KG>(a_slot, l_arow + k0 + a_k, a_group_stride,
+                                     std::make_integer_sequence<int, A_MG>{});
+    } else {
 #pragma unroll
-    for (int mg = 0; mg < A_MG; ++mg) {
-      const int row = l_m0 + mg * A_ROWS + a_m;
-      const bool row_ok = row < M;
-      const float* src_row = Ag + (row_ok ? (long long)row * lda : 0);
+      for (int mg = 0; mg < A_MG; ++mg) {
+        const int row = l_m0 + mg * A_ROWS + a_m;
+        const bool row_ok = row < M;
+        const float* src_row = Ag + (row_ok ? (long long)row * lda : 0);
 #pragma unroll
-      for (int kg = 0; kg < A_KG; ++kg) {
-        const int k = k0 + kg * kAloadK + a_k;
-        const bool ok = row_ok && (k < K);
-        ptx::cp_async_4(a_slot + (uint32_t)((kg * kAloadK * AP + mg * A_ROWS) * 4),
-                        ok ? (const void*)(src_row + k) : (const void*)Ag, ok ? 4u : 0u);
+        for (int kg = 0; kg < A_KG; ++kg) {
+          const int k = k0 + kg * kAloadK + a_k;
+          const bool ok = row_ok && (k < K);
+          ptx::cp_async_4(a_slot + (uint32_t)((kg * kAloadK * AP + mg * A_ROWS) * 4),
+                          ok ? (const void*)(src_row + k) : (const void*)Ag, ok ? 4u : 0u);
+        }
       }
     }
     if (!kBTma) {
@@ -243,24 +275,59 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     }
     ++issued;
     if (++l_k == l_ke) {
-      if (++l_piece < npieces) {
-        const Piece lp = get_piece(sc, b, l_piece);
-        int tm, tn;
-        tile_coords(sc, lp.tile, tm, tn);
-        l_k = lp.kb;
-        l_ke = lp.ke;
-        l_m0 = tm * BM;
-        l_n0 = tn * BN;
-      }
+      if (++l_piece < npieces) set_load_piece(l_piece);
     }
     return true;
   };
 
-  float acc[RM][RN];
+  // Bounded wait until both operand tiles of `step` have landed.
+  auto wait_full = [&](int step) -> bool {
+    const int slot = step % ST;
+    const uint32_t par = (uint32_t)((step / ST) & 1);
+    bool ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
+                           kDevTimeoutFull, p.timeout_ns);
+    if (kBTma && ok)
+      ok = bounded_wait(ptx::smem_addr(&bb->fullB[slot]), par, abort_w, p.status,
+                        kDevTimeoutFull, p.timeout_ns);
+    return __all_sync(FULL, ok);
+  };
+
+  // Accumulators, stored as pairs along m: acc2[i/2][j] holds rows i and i+1
+  // of column j (the operand layout of the paired FMA; the scalar orders use
+  // the two halves separately).
+  static_assert(RM % 2 == 0, "paired accumulators need an even row count");
+  float2 acc2[RM / 2][RN];
 #pragma unroll
-  for (int i = 0; i < RM; ++i)
+  for (int i = 0; i < RM / 2; ++i)
 #pragma unroll
-    for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < RN; ++j) acc2[i][j] = make_float2(0.f, 0.f);
+#define SG_ACC(i, j) (((i) & 1) ? acc2[(i) >> 1][j].y : acc2[(i) >> 1][j].x)
+
+  // Two fragment buffers: while the FFMAs of k-step k read one, the 128-bit
+  // loads of k-step k+1 fill the other.
+  float af[2][RM], bfr[2][RN];
+  auto load_frags = [&](int buf, const float* a_row, const float* b_row) {
+#pragma unroll
+    for (int wm = 0; wm < WMITER; ++wm)
+#pragma unroll
+      for (int q = 0; q < TM / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(a_row + wm * WSUBM + q * 4);
+        af[buf][wm * TM + q * 4 + 0] = v.x;
+        af[buf][wm * TM + q * 4 + 1] = v.y;
+        af[buf][wm * TM + q * 4 + 2] = v.z;
+        af[buf][wm * TM + q * 4 + 3] = v.w;
+      }
+#pragma unroll
+    for (int wn = 0; wn < WNITER; ++wn)
+#pragma unroll
+      for (int q = 0; q < TN / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4*>(b_row + wn * WSUBN + q * 4);
+        bfr[buf][wn * TN + q * 4 + 0] = v.x;
+        bfr[buf][wn * TN + q * 4 + 1] = v.y;
+        bfr[buf][wn * TN + q * 4 + 2] = v.z;
+        bfr[buf][wn * TN + q * 4 + 3] = v.w;
+      }
+  };
 
   uint32_t sync_phase = 0;
   // CTA-wide rendezvous with a bounded wait (a plain __syncthreads could not
@@ -287,6 +354,12 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     cpc = get_piece(sc, b, 0);
     c_k = cpc.kb;
   }
+  if (!aborted && nsteps > 0) {
+    if (wait_full(0))
+      load_frags(0, As + a_frag_off, Bs + b_frag_off);
+    else
+      aborted = true;
+  }
 
   for (int step = 0; step < nsteps && !aborted; ++step) {
     if (issued < nsteps) {
@@ -296,79 +369,60 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
       }
     }
     const int slot = step % ST;
-    const uint32_t par = (uint32_t)((step / ST) & 1);
-    {
-      bool ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
-                             kDevTimeoutFull, p.timeout_ns);
-      if (kBTma && ok)
-        ok = bounded_wait(ptx::smem_addr(&bb->fullB[slot]), par, abort_w, p.status,
-                          kDevTimeoutFull, p.timeout_ns);
-      if (!__all_sync(FULL, ok)) {
-        aborted = true;
-        break;
-      }
-    }
-
-    // ---- BK k-steps of outer-product FFMA on this slot -----------------------
     const float* a_s = As + slot * A_ST + a_frag_off;
     const float* b_s = Bs + slot * B_ST + b_frag_off;
-    float af[2][RM], bfr[2][RN];
+    bool next_ok = true;
+
+    // ---- BK k-steps of outer-product FFMA on this slot, KU per chunk ----------
+#pragma unroll 1
+    for (int kc = 0; kc < BK; kc += KU) {
 #pragma unroll
-    for (int wm = 0; wm < WMITER; ++wm)
+      for (int kk = 0; kk < KU; ++kk) {
+        const int cur = kk & 1, nxt = cur ^ 1;
+        if (kk + 1 < KU) {
+          load_frags(nxt, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BN);
+        } else if (kc + KU < BK) {
+          load_frags(nxt, a_s + (kc + KU) * AP, b_s + (kc + KU) * BN);
+        } else if (step + 1 < nsteps) {
+          // first k-step of the next slot, fetched under this k-step's FFMAs
+          next_ok = wait_full(step + 1);
+          const int ns = (step + 1) % ST;
+          load_frags(nxt, As + ns * A_ST + a_frag_off, Bs + ns * B_ST + b_frag_off);
+        }
+        if constexpr (S.ORDER == 2) {
+          // paired FMA: two rows of one column per instruction; the A pair
+          // comes straight from the 128-bit fragment load, the B value is
+          // duplicated into both halves
+          float2 bd[RN];
 #pragma unroll
-      for (int q = 0; q < TM / 4; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(a_s + wm * WSUBM + q * 4);
-        af[0][wm * TM + q * 4 + 0] = v.x;
-        af[0][wm * TM + q * 4 + 1] = v.y;
-        af[0][wm * TM + q * 4 + 2] = v.z;
-        af[0][wm * TM + q * 4 + 3] = v.w;
-      }
+          for (int j = 0; j < RN; ++j) bd[j] = make_float2(bfr[cur][j], bfr[cur][j]);
 #pragma unroll
-    for (int wn = 0; wn < WNITER; ++wn)
+          for (int ip = 0; ip < RM / 2; ++ip) {
+            const float2 a2 = make_float2(af[cur][2 * ip], af[cur][2 * ip + 1]);
 #pragma unroll
-      for (int q = 0; q < TN / 4; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(b_s + wn * WSUBN + q * 4);
-        bfr[0][wn * TN + q * 4 + 0] = v.x;
-        bfr[0][wn * TN + q * 4 + 1] = v.y;
-        bfr[0][wn * TN + q * 4 + 2] = v.z;
-        bfr[0][wn * TN + q * 4 + 3] = v.w;
-      }
-#pragma unroll
-    for (int k = 0; k < BK; ++k) {
-      const int cur = k & 1, nxt = cur ^ 1;
-      if (k + 1 < BK) {
-#pragma unroll
-        for (int wm = 0; wm < WMITER; ++wm)
-#pragma unroll
-          for (int q = 0; q < TM / 4; ++q) {
-            const float4 v =
-                *reinterpret_cast<const float4*>(a_s + (k + 1) * AP + wm * WSUBM + q * 4);
-            af[nxt][wm * TM + q * 4 + 0] = v.x;
-            af[nxt][wm * TM + q * 4 + 1] = v.y;
-            af[nxt][wm * TM + q * 4 + 2] = v.z;
-            af[nxt][wm * TM + q * 4 + 3] = v.w;
+            for (int j = 0; j < RN; ++j) acc2[ip][j] = __ffma2_rn(a2, bd[j], acc2[ip][j]);
           }
+        } else {
+          // scalar outer product; ORDER 1 walks odd rows backwards so that
+          // consecutive FFMAs at a row change still share their B operand
 #pragma unroll
-        for (int wn = 0; wn < WNITER; ++wn)
+          for (int i = 0; i < RM; ++i)
 #pragma unroll
-          for (int q = 0; q < TN / 4; ++q) {
-            const float4 v =
-                *reinterpret_cast<const float4*>(b_s + (k + 1) * BN + wn * WSUBN + q * 4);
-            bfr[nxt][wn * TN + q * 4 + 0] = v.x;
-            bfr[nxt][wn * TN + q * 4 + 1] = v.y;
-            bfr[nxt][wn * TN + q * 4 + 2] = v.z;
-            bfr[nxt][wn * TN + q * 4 + 3] = v.w;
-          }
+            for (int jj = 0; jj < RN; ++jj) {
+              const int j = (S.ORDER == 1 && (i & 1)) ? RN - 1 - jj : jj;
+              SG_ACC(i, j) = fmaf(af[cur][i], bfr[cur][j], SG_ACC(i, j));
+            }
+        }
       }
-#pragma unroll
-      for (int i = 0; i < RM; ++i)
-#pragma unroll
-        for (int j = 0; j < RN; ++j) acc[i][j] = fmaf(af[cur][i], bfr[cur][j], acc[i][j]);
     }
 
     // release the slot: one arrival per warp once all its lanes are done
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bb->empty[slot]));
+    if (!next_ok) {
+      aborted = true;
+      break;
+    }
 
     if (++c_k < cpc.ke) continue;
 
@@ -381,8 +435,8 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 #pragma unroll
         for (int j4 = 0; j4 < RN / 4; ++j4)
           __stcg(dst + (i * (RN / 4) + j4) * NT + tid,
-                 make_float4(acc[i][j4 * 4 + 0], acc[i][j4 * 4 + 1], acc[i][j4 * 4 + 2],
-                             acc[i][j4 * 4 + 3]));
+                 make_float4(SG_ACC(i, j4 * 4 + 0), SG_ACC(i, j4 * 4 + 1), SG_ACC(i, j4 * 4 + 2),
+                             SG_ACC(i, j4 * 4 + 3)));
       if (!cta_sync()) {
         aborted = true;
         break;
@@ -422,10 +476,10 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 #pragma unroll
             for (int j4 = 0; j4 < RN / 4; ++j4) {
               const float4 v = __ldcg(src + (i * (RN / 4) + j4) * NT + tid);
-              acc[i][j4 * 4 + 0] += v.x;
-              acc[i][j4 * 4 + 1] += v.y;
-              acc[i][j4 * 4 + 2] += v.z;
-              acc[i][j4 * 4 + 3] += v.w;
+              SG_ACC(i, j4 * 4 + 0) += v.x;
+              SG_ACC(i, j4 * 4 + 1) += v.y;
+              SG_ACC(i, j4 * 4 + 2) += v.z;
+              SG_ACC(i, j4 * 4 + 3) += v.w;
             }
         }
       }
@@ -442,13 +496,15 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
           const int row = row0 + wm * WSUBM + i;
           if (row >= M) continue;
           float* crow = p.C + (long long)row * p.ldc;
-          const float* a = acc[wm * TM + i];
+          const int ai = wm * TM + i;
 #pragma unroll
           for (int wn = 0; wn < WNITER; ++wn)
 #pragma unroll
             for (int q = 0; q < TN / 4; ++q) {
               const int col = col0 + wn * WSUBN + q * 4;
-              const float* r = a + wn * TN + q * 4;
+              const int cj = wn * TN + q * 4;
+              const float r[4] = {SG_ACC(ai, cj), SG_ACC(ai, cj + 1), SG_ACC(ai, cj + 2),
+                                  SG_ACC(ai, cj + 3)};
               if (p.c_vec && col + 3 < N) {
                 float4 v;
                 if (beta != 0.f) {
@@ -474,9 +530,9 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
         }
     }
 #pragma unroll
-    for (int i = 0; i < RM; ++i)
+    for (int i = 0; i < RM / 2; ++i)
 #pragma unroll
-      for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < RN; ++j) acc2[i][j] = make_float2(0.f, 0.f);
     if (++c_piece < npieces) {
       cpc = get_piece(sc, b, c_piece);
       c_k = cpc.kb;
@@ -500,6 +556,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     }
     __nanosleep(20000);
   }
+#undef SG_ACC
 }
 
 }  // namespace sgemm_gb300

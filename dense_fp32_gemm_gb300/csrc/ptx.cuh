@@ -53,6 +53,14 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
                : "memory");
 }
 
+// Unpredicated 4-byte copy with immediate offsets on both addresses.
+template <int DST_OFF, int SRC_OFF>
+__device__ __forceinline__ void cp_async_4_imm(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0+%2], [%1+%3], 4;" ::"r"(dst), "l"(src), "n"(DST_OFF),
+               "n"(SRC_OFF)
+               : "memory");
+}
+
 // Arrives on `bar` once every cp.async this thread issued so far has landed.
 // The barrier's expected count must include this arrival (no increment).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -39,6 +39,9 @@ struct TileShape {
   int NT;                // threads per CTA
   int STAGES;            // shared-memory pipeline depth
   int MINB;              // CTAs per SM promised to the register allocator
+  int KU;                // k-steps per unrolled chunk of the inner loop
+  int ORDER;             // k-step update: 0 FFMA row by row, 1 FFMA zig-zag,
+                         // 2 paired FMA (two rows of a column per instruction)
 };
 
 // Derived quantities; valid only for shapes that pass cfg_valid().
@@ -51,9 +54,11 @@ constexpr int est_registers(const TileShape& s) {
 }
 constexpr int a_stage_floats(const TileShape& s) { return s.BK * (s.BM + kApad); }
 constexpr int b_stage_floats(const TileShape& s) { return s.BK * s.BN; }
-// Stage buffers, then 3 mbarriers per stage (A landed, B landed, slot free).
+// Dynamic shared memory of one CTA: 1024 bytes of alignment slack, the stage
+// buffers, then 3 mbarriers per stage (A landed, B landed, slot free), one
+// rendezvous barrier and an abort word.
 constexpr int smem_bytes(const TileShape& s) {
-  return s.STAGES * (a_stage_floats(s) + b_stage_floats(s)) * 4 + s.STAGES * 3 * 8 + 16;
+  return 1024 + s.STAGES * (a_stage_floats(s) + b_stage_floats(s)) * 4 + s.STAGES * 3 * 8 + 16;
 }
 
 // Every assumption of the kernel in ffma_sgemm.cuh, in the order the kernel
@@ -62,7 +67,8 @@ constexpr int smem_bytes(const TileShape& s) {
 constexpr int cfg_check(const TileShape& s) {
   // 1. positive extents
   if (s.BM <= 0 || s.BN <= 0 || s.BK <= 0 || s.WM <= 0 || s.WN <= 0 || s.WNITER <= 0 ||
-      s.TM <= 0 || s.TN <= 0 || s.NT <= 0 || s.STAGES <= 0 || s.MINB <= 0)
+      s.TM <= 0 || s.TN <= 0 || s.NT <= 0 || s.STAGES <= 0 || s.MINB <= 0 || s.KU <= 0 ||
+      s.ORDER < 0 || s.ORDER > 2)
     return 1;
   // 2. whole warps, and warp tiles that tile the CTA tile one warp each
   if (s.NT % kWarp != 0) return 2;
@@ -100,6 +106,9 @@ constexpr int cfg_check(const TileShape& s) {
   //     64K-entry register file of an SM
   if (est_registers(s) > 255) return 20;
   if (s.NT * s.MINB * est_registers(s) > 65536) return 21;
+  // 12. the inner loop runs BK/KU chunks of KU fully unrolled k-steps; the
+  //     two fragment buffers alternate inside a chunk, so KU must be even
+  if (s.KU % 2 != 0 || s.BK % s.KU != 0) return 22;
   return 0;
 }
 

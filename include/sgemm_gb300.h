@@ -91,7 +91,9 @@ void sgemm_shutdown(void);
  * Tile configurations compiled into the library. sgemm_config_count() gives
  * their number; sgemm_config_info() fills name (len bytes) and the tile
  * parameters of configuration `id` as
- * {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB} in params[11].
+ * {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB, KU, ORDER} in
+ * params[13] (KU: k-steps per unrolled chunk; ORDER: 0 row-by-row FFMA, 1 zig-zag
+ * FFMA, 2 paired FMA).
  */
 int sgemm_config_count(void);
 int sgemm_config_info(int id, char* name, int len, int* params);
@@ -106,7 +108,7 @@ int sgemm_force_config(int id);
  * The legality checker of the tile configurations, evaluated on the host:
  * 0 if the tuple is legal for the FFMA kernel, else the number of the first
  * rule it breaks. params = {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES,
- * MINB}. derived (if not NULL) receives {WMITER, WSUBM, WSUBN, accumulators
+ * MINB, KU, ORDER}. derived (if not NULL) receives {WMITER, WSUBM, WSUBN, accumulators
  * per thread, shared bytes per CTA} when the tuple is legal.
  */
 int sgemm_cfg_check(const int* params, int* derived);

@@ -18,8 +18,8 @@ from dense_fp32_gemm_gb300 import binding
 GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_analytic.json")))
 
 
-def P(BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES=3, MINB=1):
-    return [BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB]
+def P(BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES=3, MINB=1, KU=4, ORDER=0):
+    return [BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB, KU, ORDER]
 
 
 def test_pages_winner_derived_values():
@@ -34,7 +34,7 @@ def test_pages_winner_derived_values():
 
 
 def test_default_config_derived_values():
-    rule, d = binding.sgemm_cfg_check(P(128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1))
+    rule, d = binding.sgemm_cfg_check(P(128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1, 4, 0))
     assert rule == 0 and d["WMITER"] == 4 and d["acc"] == 128
 
 
@@ -57,6 +57,8 @@ BAD = [
     (P(128, 256, 16, 64, 64, 2, 4, 4, 256, 6, 2), 18),# shared memory per SM
     (P(256, 128, 16, 128, 64, 2, 4, 4, 128, 3, 1), 19),# 256 accumulators
     (P(128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 5), 21), # register file at 5 CTAs/SM
+    (P(128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1, 3), 22),  # odd unroll chunk
+    (P(128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1, 32), 22), # chunk deeper than BK
 ]
 
 
@@ -66,6 +68,7 @@ def test_illegal_tuples_name_their_rule(params, rule):
 
 
 def test_no_division_by_zero_on_degenerate_tuples():
-    for bad in ([0] * 11, [1] * 11, [128, 64, 16, 0, 0, 0, 0, 0, 128, 3, 1],
-                [-128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1]):
+    for bad in ([0] * 13, [1] * 13, [128, 64, 16, 0, 0, 0, 0, 0, 128, 3, 1, 4, 0],
+                [-128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1, 4, 0],
+                [128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1, 4, 3]):
         assert binding.sgemm_cfg_check(bad)[0] != 0

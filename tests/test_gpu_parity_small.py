@@ -10,10 +10,11 @@ from dense_fp32_gemm_gb300 import binding
 from dense_fp32_gemm_gb300.workloads import WORKLOADS, Workload, make_inputs
 
 import gpu_helpers as H
+from conftest import compiled_config_count
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = list(range(4))
+CONFIGS = list(range(compiled_config_count()))
 
 SHAPES = [
     (128, 128, 128), (1, 1, 1), (1, 300, 5), (300, 1, 5), (7, 9, 3), (33, 65, 17),
