@@ -66,8 +66,12 @@ def ffma_peak_tflops(sms, mhz):
 
 
 def kernel_source_hash():
+    """Hash of the sources that define the GEMM kernels (the C-ABI file,
+    which only validates and dispatches, is left out)."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_gemm_gb300", "csrc", "*"))):
+        if os.path.basename(f) == "api.cu":
+            continue
         h.update(os.path.basename(f).encode())
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
@@ -80,9 +84,10 @@ def measured_peaks():
         return {}
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, tile_config):
     """DRAM bytes per launch from the committed ncu summary of this workload,
-    or None if there is none or the kernel sources changed since."""
+    or None if there is none, the kernel sources changed since, or the
+    summary was taken on another tile configuration."""
     path = os.path.join(ROOT, "profiles", f"ffma_sgemm_{workload}.md")
     try:
         text = open(path).read()
@@ -90,7 +95,10 @@ def profiled_traffic(workload):
         return None
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    c = re.search(r"tile_config:\s*(\S+)", text)
     if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    if not c or not tile_config.startswith(c.group(1)):
         return None
     return float(m.group(1))
 
@@ -342,7 +350,7 @@ def run_ours(args, w):
     max_mhz = float(peaks.get("sm_max_mhz") or (clocks or {}).get("sm_max_mhz") or 2070.0)
     peak_tf = ffma_peak_tflops(sms, max_mhz)
     achieved_tf = gemm_flops(w.M, w.N, w.K) / kern_s / 1e12
-    traffic = profiled_traffic(w.name)
+    traffic = profiled_traffic(w.name, tile_config)
     sampled = (clocks or {}).get("sm_mhz")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,

@@ -148,8 +148,8 @@ int get_workspace(int dev, cudaStream_t stream, size_t flags, size_t partial_flo
 int choose_config(int M, int N, int K, int sms) {
   (void)K;
   (void)sms;
-  if (N <= 96) return kIdTallBk24;
-  return kIdWideBk32F2;
+  if (N <= 96) return kIdTallBk24F2;
+  return kIdWideBk32F2Ku16;
 }
 
 __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {

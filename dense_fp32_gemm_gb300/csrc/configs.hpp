@@ -42,7 +42,8 @@ struct KernelParams;
   X(WideBk48F2, 128, 256, 48, 64, 64, 2, 4, 4, 256, 3, 1, 8, 2)    \
   X(WideBk16F2, 128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1, 8, 2)    \
   X(SquareBk32F2, 128, 128, 32, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)  \
-  X(TallBk24F2, 256, 64, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)
+  X(TallBk24F2, 256, 64, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)     \
+  X(WideBk32F2Ku16, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 16, 2)
 
 #define SGEMM_GB300_CFG_STRUCT(NAME, BM, BN, BK, WM, WN, WNI, TM, TN, NT, ST, MINB, KU, OR)     \
   struct Cfg##NAME {                                                                            \

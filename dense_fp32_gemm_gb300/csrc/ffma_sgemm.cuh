@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   constexpr TileShape S = Cfg::S;
   static_assert(cfg_valid(S), "illegal tile configuration");
   constexpr int BM = S.BM, BN = S.BN, BK = S.BK, NT = S.NT, ST = S.STAGES, KU = S.KU;
+  constexpr int ORDER = S.ORDER;
   constexpr int WM = S.WM, WN = S.WN, TM = S.TM, TN = S.TN, WNITER = S.WNITER;
   constexpr int WMITER = wmiter(S), WSUBM = wsubm(S), WSUBN = wsubn(S);
   constexpr int AP = BM + kApad;               // As row pitch (floats)
@@ -280,15 +281,28 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     return true;
   };
 
-  // Bounded wait until both operand tiles of `step` have landed.
-  auto wait_full = [&](int step) -> bool {
+  // Non-blocking test: have both operand tiles of `step` landed? (Both
+  // barriers are polled at once so their latencies overlap.)
+  auto test_full = [&](int step) -> bool {
     const int slot = step % ST;
     const uint32_t par = (uint32_t)((step / ST) & 1);
-    bool ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
-                           kDevTimeoutFull, p.timeout_ns);
-    if (kBTma && ok)
-      ok = bounded_wait(ptx::smem_addr(&bb->fullB[slot]), par, abort_w, p.status,
+    const bool a = ptx::mbar_try_wait(ptx::smem_addr(&bb->fullA[slot]), par);
+    const bool b2 = kBTma ? ptx::mbar_try_wait(ptx::smem_addr(&bb->fullB[slot]), par) : true;
+    return a && b2;
+  };
+  // Bounded wait until both operand tiles of `step` have landed; `ready` is
+  // the result of an earlier test_full(step), if one was made.
+  auto wait_full = [&](int step, bool ready) -> bool {
+    bool ok = true;
+    if (!ready) {
+      const int slot = step % ST;
+      const uint32_t par = (uint32_t)((step / ST) & 1);
+      ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
                         kDevTimeoutFull, p.timeout_ns);
+      if (kBTma && ok)
+        ok = bounded_wait(ptx::smem_addr(&bb->fullB[slot]), par, abort_w, p.status,
+                          kDevTimeoutFull, p.timeout_ns);
+    }
     return __all_sync(FULL, ok);
   };
 
@@ -355,7 +369,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     c_k = cpc.kb;
   }
   if (!aborted && nsteps > 0) {
-    if (wait_full(0))
+    if (wait_full(0, false))
       load_frags(0, As + a_frag_off, Bs + b_frag_off);
     else
       aborted = true;
@@ -373,46 +387,63 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     const float* b_s = Bs + slot * B_ST + b_frag_off;
     bool next_ok = true;
 
-    // ---- BK k-steps of outer-product FFMA on this slot, KU per chunk ----------
+    // ---- BK k-steps of outer-product FMA on this slot, KU per chunk ----------
+    // One k-step: update the accumulators from fragment buffer `cur`.
+    auto kstep = [&](int cur) {
+      if constexpr (ORDER == 2) {
+        // paired FMA: two rows of one column per instruction; the A pair
+        // comes straight from the 128-bit fragment load, the B value is
+        // duplicated into both halves
+        float2 bd[RN];
+#pragma unroll
+        for (int j = 0; j < RN; ++j) bd[j] = make_float2(bfr[cur][j], bfr[cur][j]);
+#pragma unroll
+        for (int ip = 0; ip < RM / 2; ++ip) {
+          const float2 a2 = make_float2(af[cur][2 * ip], af[cur][2 * ip + 1]);
+#pragma unroll
+          for (int j = 0; j < RN; ++j) acc2[ip][j] = __ffma2_rn(a2, bd[j], acc2[ip][j]);
+        }
+      } else {
+        // scalar outer product; ORDER 1 walks odd rows backwards so that
+        // consecutive FFMAs at a row change still share their B operand
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+          for (int jj = 0; jj < RN; ++jj) {
+            const int j = (ORDER == 1 && (i & 1)) ? RN - 1 - jj : jj;
+            SG_ACC(i, j) = fmaf(af[cur][i], bfr[cur][j], SG_ACC(i, j));
+          }
+      }
+    };
+
+    // all chunks but the last: the next fragment always comes from this slot
 #pragma unroll 1
-    for (int kc = 0; kc < BK; kc += KU) {
+    for (int kc = 0; kc < BK - KU; kc += KU) {
 #pragma unroll
       for (int kk = 0; kk < KU; ++kk) {
-        const int cur = kk & 1, nxt = cur ^ 1;
+        const int cur = kk & 1;
+        load_frags(cur ^ 1, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BN);
+        kstep(cur);
+      }
+    }
+    // last chunk: halfway through, test whether the next slot has landed;
+    // in the last k-step, fetch its first fragment under this k-step's FMAs
+    {
+      constexpr int kc = BK - KU;
+      const bool has_next = step + 1 < nsteps;
+      bool ready = false;
+#pragma unroll
+      for (int kk = 0; kk < KU; ++kk) {
+        const int cur = kk & 1;
         if (kk + 1 < KU) {
-          load_frags(nxt, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BN);
-        } else if (kc + KU < BK) {
-          load_frags(nxt, a_s + (kc + KU) * AP, b_s + (kc + KU) * BN);
-        } else if (step + 1 < nsteps) {
-          // first k-step of the next slot, fetched under this k-step's FFMAs
-          next_ok = wait_full(step + 1);
+          load_frags(cur ^ 1, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BN);
+          if (kk == KU / 2 - 1 && has_next) ready = test_full(step + 1);
+        } else if (has_next) {
+          next_ok = wait_full(step + 1, ready);
           const int ns = (step + 1) % ST;
-          load_frags(nxt, As + ns * A_ST + a_frag_off, Bs + ns * B_ST + b_frag_off);
+          load_frags(cur ^ 1, As + ns * A_ST + a_frag_off, Bs + ns * B_ST + b_frag_off);
         }
-        if constexpr (S.ORDER == 2) {
-          // paired FMA: two rows of one column per instruction; the A pair
-          // comes straight from the 128-bit fragment load, the B value is
-          // duplicated into both halves
-          float2 bd[RN];
-#pragma unroll
-          for (int j = 0; j < RN; ++j) bd[j] = make_float2(bfr[cur][j], bfr[cur][j]);
-#pragma unroll
-          for (int ip = 0; ip < RM / 2; ++ip) {
-            const float2 a2 = make_float2(af[cur][2 * ip], af[cur][2 * ip + 1]);
-#pragma unroll
-            for (int j = 0; j < RN; ++j) acc2[ip][j] = __ffma2_rn(a2, bd[j], acc2[ip][j]);
-          }
-        } else {
-          // scalar outer product; ORDER 1 walks odd rows backwards so that
-          // consecutive FFMAs at a row change still share their B operand
-#pragma unroll
-          for (int i = 0; i < RM; ++i)
-#pragma unroll
-            for (int jj = 0; jj < RN; ++jj) {
-              const int j = (S.ORDER == 1 && (i & 1)) ? RN - 1 - jj : jj;
-              SG_ACC(i, j) = fmaf(af[cur][i], bfr[cur][j], SG_ACC(i, j));
-            }
-        }
+        kstep(cur);
       }
     }
 
