@@ -25,6 +25,7 @@ SGEMM_ERR_DEVICE_TIMEOUT = -6
 SGEMM_ERR_ALLOC = -7
 SGEMM_ERR_MISALIGNED = -8
 SGEMM_ERR_INVALID_VALUE = -9
+SGEMM_ERR_NOALLOC_CAPACITY = -10
 
 PARAM_NAMES = ("BM", "BN", "BK", "WM", "WN", "WNITER", "TM", "TN", "NT", "STAGES", "MINB", "KU", "ORDER")
 
@@ -66,6 +67,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_schedule_piece": (I, [IP, I, I, IP]),
                 "sgemm_diag_wait_timeout": (I, [LL, P]),
                 "sgemm_set_wait_timeout_ns": (LL, [LL]),
+                "sgemm_noalloc": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -168,6 +170,13 @@ def sgemm_diag_wait_timeout(timeout_ns: int, stream=None) -> int:
 
 def sgemm_set_wait_timeout_ns(ns: int) -> int:
     return lib().sgemm_set_wait_timeout_ns(ns)
+
+
+def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """Same call as sgemm() for callers that cannot allocate device memory:
+    the kernel's scratch comes from a fixed buffer inside the library.
+    Returns the status code."""
+    return lib().sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 # ---- torch conveniences (marshalling only) ------------------------------------------

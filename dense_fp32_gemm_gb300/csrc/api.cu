@@ -200,6 +200,8 @@ SGEMM_API const char* sgemm_status_string(int status) {
     case SGEMM_ERR_ALLOC: return "workspace allocation failed";
     case SGEMM_ERR_MISALIGNED: return "matrix pointer not 4-byte aligned";
     case SGEMM_ERR_INVALID_VALUE: return "invalid argument value";
+    case SGEMM_ERR_NOALLOC_CAPACITY:
+      return "problem needs more scratch than the fixed no-allocation buffer holds";
     default: return "unknown status";
   }
 }

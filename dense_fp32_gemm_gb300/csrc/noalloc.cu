@@ -1,0 +1,262 @@
+// noalloc.cu -- sgemm_noalloc(): the same GEMM as sgemm(), for callers that
+// must not allocate device memory.
+//
+// sgemm() allocates (once per device and stream) the scratch its kernel needs:
+// a status word, one flag per persistent CTA, and the partial tiles of the
+// K-split schedule. Some callers cannot let a library call cudaMalloc: code
+// that runs while a stream is being captured into a graph (allocation is not
+// allowed there), code inside an application whose memory pool owns every free
+// byte of the device and forbids hidden allocations, and latency-critical
+// loops that cannot absorb an allocation or its implicit synchronisation.
+// For them, this file keeps that scratch in one fixed, file-scope device
+// array. Every GPU that loads the library holds the array until the process
+// exits; nothing is allocated per call.
+//
+// Limits and sharing:
+//   * the array is kNoAllocScratchBytes (24 MiB): a 256-byte status word,
+//     flags for up to kNoAllocMaxFlags CTAs, and 24 MiB - 64 KiB of partial
+//     tiles. On a 152-SM GB300 every problem fits with the built-in tile
+//     configurations (the largest need is about 20 MB); a call whose
+//     schedule needs more returns SGEMM_ERR_NOALLOC_CAPACITY and launches
+//     nothing;
+//   * all calls share the one array and it keeps the last call's contents.
+//     The status word is cleared at the start of every call; the flags are
+//     matched against a per-device call counter, so stale flags are never
+//     mistaken for fresh ones (they are cleared whenever the counter wraps);
+//     partial tiles are always written before they are read. Calls that
+//     overlap on the GPU (two streams, or two host threads) race on the array;
+//   * the first call on a device performs its set-up: it looks up the
+//     array's device address (cudaGetSymbolAddress, with that device current)
+//     and sets the kernels' shared-memory attributes. Make that first call
+//     before any stream capture;
+//   * a kernel that gives up on a bounded wait records its code in the
+//     array's status word, which the next call clears; sgemm_poll_device_status
+//     does not see it.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sgemm_gb300.h"
+#include "configs.hpp"
+#include "ffma_sgemm.cuh"
+#include "schedule.hpp"
+#include "tile_config.hpp"
+
+#define SGEMM_API extern "C" __attribute__((visibility("default")))
+
+namespace sgemm_gb300 {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;
+constexpr size_t kNoAllocHeaderBytes = size_t(64) << 10;  // status word + flags
+constexpr size_t kNoAllocStatusBytes = 256;
+constexpr size_t kNoAllocMaxFlags = (kNoAllocHeaderBytes - kNoAllocStatusBytes) / 4;
+constexpr int kNoAllocMaxDevices = 64;
+
+// The scratch itself. Host code must not use this name as an address: it only
+// stands for the symbol; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+#define SGEMM_GB300_NOALLOC_PTR(NAME, ...) &kEntry##NAME,
+const ConfigEntry* const kNoAllocConfigs[] = {SGEMM_GB300_CONFIGS(SGEMM_GB300_NOALLOC_PTR)};
+#undef SGEMM_GB300_NOALLOC_PTR
+constexpr int kNoAllocNumConfigs = sizeof(kNoAllocConfigs) / sizeof(kNoAllocConfigs[0]);
+#define SGEMM_GB300_NOALLOC_ID(NAME, ...) kNa##NAME,
+enum : int { SGEMM_GB300_CONFIGS(SGEMM_GB300_NOALLOC_ID) kNaCount };
+#undef SGEMM_GB300_NOALLOC_ID
+
+struct NoAllocDevice {
+  bool ready;
+  int sms;
+  int occupancy[kNoAllocNumConfigs][2];
+  unsigned char* base;  // device address of g_noalloc_scratch on this device
+  uint32_t epoch;
+};
+
+std::mutex g_na_mutex;
+NoAllocDevice g_na_devices[kNoAllocMaxDevices];  // fixed storage: no heap use
+PFN_cuTensorMapEncodeTiled_v12000 g_na_encode = nullptr;
+bool g_na_encode_tried = false;
+
+// Same rule and schedule constants as the automatic choice of sgemm(), so
+// both entry points run the same kernel with the same schedule.
+constexpr int kNaGroupM = 8;
+constexpr int kNaMinSplitUnits = 4;
+int noalloc_choose_config(int N) { return N <= 96 ? kNaTallBk24F2 : kNaWideBk32F2Ku16; }
+
+// Once per device, with that device current: symbol address, kernel
+// attributes, occupancy. Called with g_na_mutex held.
+int noalloc_setup(int dev, NoAllocDevice** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+  NoAllocDevice& d = g_na_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+    if (!(major == 10 && minor == 3)) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+    for (int c = 0; c < kNoAllocNumConfigs; ++c) {
+      if (kNoAllocConfigs[c]->set_attributes() != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+      }
+      for (int t = 0; t < 2; ++t) {
+        int blocks = 0;
+        if (kNoAllocConfigs[c]->occupancy(t != 0, &blocks) != cudaSuccess) {
+          cudaGetLastError();
+          return SGEMM_ERR_LAUNCH;
+        }
+        d.occupancy[c][t] = blocks;
+      }
+    }
+    d.base = static_cast<unsigned char*>(ptr);
+    d.epoch = 0;
+    d.ready = true;
+  }
+  *out = &d;
+  return SGEMM_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 noalloc_encoder() {
+  if (!g_na_encode_tried) {
+    g_na_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_na_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_na_encode;
+}
+
+__global__ void noalloc_scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {
+  const long long total = (long long)M * N;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long i = e / N, j = e % N;
+    float* c = C + i * ldc + j;
+    *c = beta == 0.f ? 0.f : beta * *c;
+  }
+}
+
+}  // namespace
+}  // namespace sgemm_gb300
+
+using namespace sgemm_gb300;
+
+SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, int lda,
+                            const float* B, int ldb, float beta, float* C, int ldc,
+                            void* stream_) {
+  // argument checks: identical to sgemm(), nothing launched on error
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return SGEMM_ERR_INVALID_LD;
+  if (M == 0 || N == 0) return SGEMM_OK;
+  const bool reads_ab = (K > 0 && alpha != 0.f);
+  if (C == nullptr || (reads_ab && (A == nullptr || B == nullptr))) return SGEMM_ERR_NULL_PTR;
+  if ((reinterpret_cast<uintptr_t>(C) & 3u) ||
+      (reads_ab && ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))))
+    return SGEMM_ERR_MISALIGNED;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  NoAllocDevice* d = nullptr;
+  int st = noalloc_setup(dev, &d);
+  if (st != SGEMM_OK) return st;
+
+  if (!reads_ab) {
+    const long long total = (long long)M * N;
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > d->sms * 8) blocks = d->sms * 8;
+    noalloc_scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+  }
+
+  const int id = noalloc_choose_config(N);
+  const ConfigEntry& cfg = *kNoAllocConfigs[id];
+  const TileShape& S = cfg.shape;
+
+  bool tma = ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) && ((ldb & 3) == 0);
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (tma) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = noalloc_encoder();
+    tma = false;
+    if (enc != nullptr) {
+      cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+      cuuint64_t strides[1] = {(cuuint64_t)ldb * 4};
+      cuuint32_t box[2] = {(cuuint32_t)S.BN, (cuuint32_t)S.BK};
+      cuuint32_t estr[2] = {1, 1};
+      tma = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+  }
+
+  const int occ = d->occupancy[id][tma ? 1 : 0];
+  if (occ < 1) return SGEMM_ERR_LAUNCH;
+  const Schedule sched =
+      make_schedule((M + S.BM - 1) / S.BM, (N + S.BN - 1) / S.BN, (K + S.BK - 1) / S.BK,
+                    d->sms * occ, kNaGroupM, kNaMinSplitUnits);
+  const bool split = sched.dp_tiles < sched.tiles;
+  const size_t partial_bytes = split ? (size_t)sched.grid * S.BM * S.BN * 4 : 0;
+  if ((size_t)sched.grid > kNoAllocMaxFlags ||
+      partial_bytes > kNoAllocScratchBytes - kNoAllocHeaderBytes)
+    return SGEMM_ERR_NOALLOC_CAPACITY;
+
+  int* status = reinterpret_cast<int*>(d->base);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(d->base + kNoAllocStatusBytes);
+  float* partials = reinterpret_cast<float*>(d->base + kNoAllocHeaderBytes);
+  // the status word starts every call at zero; the flags only on a wrap of
+  // the call counter (a flag is fresh when it equals this call's number)
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  if (++d->epoch == 0) {
+    d->epoch = 1;
+    if (cudaMemsetAsync(flags, 0, kNoAllocMaxFlags * 4, stream) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+  }
+
+  KernelParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  p.sched = sched;
+  p.ws = partials;
+  p.flags = flags;
+  p.status = status;
+  p.epoch = d->epoch;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && ((ldc & 3) == 0);
+  p.timeout_ns = 4000000000LL;
+  if (cfg.launch(tma, sched.grid, p, &map, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  return SGEMM_OK;
+}

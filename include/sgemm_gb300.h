@@ -48,7 +48,9 @@ typedef enum {
   SGEMM_ERR_DEVICE_TIMEOUT = -6,    /* a kernel gave up on a bounded wait         */
   SGEMM_ERR_ALLOC = -7,             /* workspace allocation failed                */
   SGEMM_ERR_MISALIGNED = -8,        /* a matrix pointer is not 4-byte aligned     */
-  SGEMM_ERR_INVALID_VALUE = -9      /* other invalid argument (config id, buffer) */
+  SGEMM_ERR_INVALID_VALUE = -9,     /* other invalid argument (config id, buffer) */
+  SGEMM_ERR_NOALLOC_CAPACITY = -10  /* sgemm_noalloc: problem needs more scratch
+                                       than its fixed buffer holds             */
 } sgemm_status;
 
 /*
@@ -141,6 +143,30 @@ int sgemm_diag_wait_timeout(long long timeout_ns, void* stream);
  * 4e9). Values < 1000 are rejected. Returns the previous value or a negative
  * status. */
 long long sgemm_set_wait_timeout_ns(long long ns);
+
+/*
+ * The same C = alpha * A * B + beta * C as sgemm(), with the same arguments,
+ * checks and results, for callers that must not allocate device memory: code
+ * running while a stream is captured into a graph, applications whose memory
+ * pool owns every free byte and forbids hidden allocations, and latency-bound
+ * loops that cannot absorb an allocation. The pages have no counterpart; this
+ * is a packaging of the same kernel.
+ *
+ * The kernel's scratch (status word, one flag per persistent CTA, split-K
+ * partial tiles) lives in one fixed 24 MiB device array inside the library,
+ * which every GPU that loads the library holds until the process exits; no
+ * call allocates. The first call on a device does the set-up (the array's
+ * device address, the kernels' attributes): make it before any stream
+ * capture. A problem whose schedule needs more scratch than the array holds
+ * returns SGEMM_ERR_NOALLOC_CAPACITY and launches nothing (on a 152-SM GB300
+ * every problem fits). All calls share the array: calls that overlap on the
+ * GPU (other streams, other host threads) race and must not be issued. The
+ * device status of these calls is kept in the array and cleared by the next
+ * call; sgemm_poll_device_status() does not report it. The tile configuration
+ * is always the automatic choice (sgemm_force_config() does not apply).
+ */
+int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                  int ldb, float beta, float* C, int ldc, void* stream);
 
 #ifdef __cplusplus
 }
