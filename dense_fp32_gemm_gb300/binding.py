@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_diag_wait_timeout": (I, [LL, P]),
                 "sgemm_set_wait_timeout_ns": (LL, [LL]),
                 "sgemm_noalloc": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_choose_config": (I, [I, I, I, IP]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -128,6 +129,18 @@ def sgemm_config_info(cid: int):
 
 def sgemm_force_config(cid: int) -> int:
     return lib().sgemm_force_config(cid)
+
+
+SHAPE_CLASSES = ("square_large", "square_small", "k_dominant", "skinny_n", "skinny_m")
+
+
+def sgemm_choose_config(M, N, K):
+    """(config id, shape class name) of the automatic choice."""
+    cls = ctypes.c_int(-1)
+    cid = lib().sgemm_choose_config(M, N, K, ctypes.byref(cls))
+    if cid < 0:
+        raise SgemmError(cid, "sgemm_choose_config")
+    return cid, SHAPE_CLASSES[cls.value]
 
 
 def sgemm_cfg_check(params):

@@ -16,6 +16,7 @@
 
 #include "../../include/sgemm_gb300.h"
 #include "configs.hpp"
+#include "dispatch.hpp"
 #include "ffma_sgemm.cuh"
 #include "schedule.hpp"
 #include "tile_config.hpp"
@@ -30,10 +31,7 @@ namespace {
 const ConfigEntry* const kConfigs[] = {SGEMM_GB300_CONFIGS(SGEMM_GB300_ENTRY_PTR)};
 #undef SGEMM_GB300_ENTRY_PTR
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
-#define SGEMM_GB300_ENTRY_ID(NAME, ...) kId##NAME,
-enum ConfigId : int { SGEMM_GB300_CONFIGS(SGEMM_GB300_ENTRY_ID) kIdCount };
-#undef SGEMM_GB300_ENTRY_ID
-static_assert(kIdCount == kNumConfigs, "config ids");
+static_assert(kNumConfigIds == kNumConfigs, "config ids");
 
 // Raster group height (tiles) and the fewest k-slices worth splitting off.
 constexpr int kGroupM = 8;
@@ -144,13 +142,6 @@ int get_workspace(int dev, cudaStream_t stream, size_t flags, size_t partial_flo
   return SGEMM_OK;
 }
 
-// Automatic choice of tile configuration by shape class.
-int choose_config(int M, int N, int K, int sms) {
-  (void)K;
-  (void)sms;
-  if (N <= 96) return kIdTallBk24F2;
-  return kIdWideBk32F2Ku16;
-}
 
 __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {
   const long long total = (long long)M * N;
@@ -241,7 +232,7 @@ SGEMM_API int sgemm(int M, int N, int K, float alpha, const float* A, int lda, c
   }
 
   int id = g_forced.load();
-  if (id < 0 || id >= kNumConfigs) id = choose_config(M, N, K, di->sms);
+  if (id < 0 || id >= kNumConfigs) id = choose_config(M, N, K);
   const ConfigEntry& cfg = *kConfigs[id];
   const TileShape& S = cfg.shape;
 
@@ -445,4 +436,10 @@ SGEMM_API int sgemm_diag_wait_timeout(long long timeout_ns, void* stream_) {
 SGEMM_API long long sgemm_set_wait_timeout_ns(long long ns) {
   if (ns < 1000) return SGEMM_ERR_INVALID_VALUE;
   return g_timeout_ns.exchange(ns);
+}
+
+SGEMM_API int sgemm_choose_config(int M, int N, int K, int* shape_class) {
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
+  if (shape_class != nullptr) *shape_class = classify_shape(M, N, K);
+  return choose_config(M, N, K);
 }

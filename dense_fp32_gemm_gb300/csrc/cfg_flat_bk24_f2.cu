@@ -1,0 +1,7 @@
+// cfg_flat_bk24_f2.cu -- instantiation of the FFMA kernel for CfgFlatBk24F2 (one translation
+// unit per configuration so that the library compiles in parallel).
+#include "launch.cuh"
+
+namespace sgemm_gb300 {
+SGEMM_GB300_DEFINE_ENTRY(CfgFlatBk24F2, kEntryFlatBk24F2)
+}  // namespace sgemm_gb300

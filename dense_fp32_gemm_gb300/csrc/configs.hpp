@@ -21,6 +21,7 @@ struct KernelParams;
 // wide:    128 x 256 CTA tile, 8 warps of 64 x 64, 16 x 8 accumulators per lane
 //          (B arrives by TMA, so a wide BN costs no loader instructions);
 // tall:    256 x 64, 4 warps of 64 x 64, for N <= 64;
+// flat:    64 x 256, 4 warps of 64 x 64, for M <= 64;
 // square:  128 x 128, 4 warps of 64 x 64, two CTAs per SM;
 // pages:   the pages' sweep winner (128 x 64 x 16, warp 64 x 32, WNITER 2,
 //          4 x 4 patches, 128 threads) on this kernel's pipeline;
@@ -43,7 +44,8 @@ struct KernelParams;
   X(WideBk16F2, 128, 256, 16, 64, 64, 2, 4, 4, 256, 4, 1, 8, 2)    \
   X(SquareBk32F2, 128, 128, 32, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)  \
   X(TallBk24F2, 256, 64, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)     \
-  X(WideBk32F2Ku16, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 16, 2)
+  X(WideBk32F2Ku16, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 16, 2) \
+  X(FlatBk24F2, 64, 256, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)
 
 #define SGEMM_GB300_CFG_STRUCT(NAME, BM, BN, BK, WM, WN, WNI, TM, TN, NT, ST, MINB, KU, OR)     \
   struct Cfg##NAME {                                                                            \
@@ -68,6 +70,11 @@ struct ConfigEntry {
   OccFn occupancy;
   LaunchFn launch;
 };
+
+// Registry index of each configuration: kId<Name>.
+#define SGEMM_GB300_CONFIG_ID(NAME, ...) kId##NAME,
+enum ConfigId : int { SGEMM_GB300_CONFIGS(SGEMM_GB300_CONFIG_ID) kNumConfigIds };
+#undef SGEMM_GB300_CONFIG_ID
 
 // Defined in the cfg_*.cu translation units, one per configuration.
 #define SGEMM_GB300_DECLARE_ENTRY(NAME, ...) extern const ConfigEntry kEntry##NAME;

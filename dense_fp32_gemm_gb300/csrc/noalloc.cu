@@ -42,6 +42,7 @@
 
 #include "../../include/sgemm_gb300.h"
 #include "configs.hpp"
+#include "dispatch.hpp"
 #include "ffma_sgemm.cuh"
 #include "schedule.hpp"
 #include "tile_config.hpp"
@@ -65,9 +66,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 const ConfigEntry* const kNoAllocConfigs[] = {SGEMM_GB300_CONFIGS(SGEMM_GB300_NOALLOC_PTR)};
 #undef SGEMM_GB300_NOALLOC_PTR
 constexpr int kNoAllocNumConfigs = sizeof(kNoAllocConfigs) / sizeof(kNoAllocConfigs[0]);
-#define SGEMM_GB300_NOALLOC_ID(NAME, ...) kNa##NAME,
-enum : int { SGEMM_GB300_CONFIGS(SGEMM_GB300_NOALLOC_ID) kNaCount };
-#undef SGEMM_GB300_NOALLOC_ID
 
 struct NoAllocDevice {
   bool ready;
@@ -82,11 +80,10 @@ NoAllocDevice g_na_devices[kNoAllocMaxDevices];  // fixed storage: no heap use
 PFN_cuTensorMapEncodeTiled_v12000 g_na_encode = nullptr;
 bool g_na_encode_tried = false;
 
-// Same rule and schedule constants as the automatic choice of sgemm(), so
-// both entry points run the same kernel with the same schedule.
+// Same schedule constants as sgemm() and the same automatic tile choice
+// (dispatch.hpp), so both entry points run the same kernel and schedule.
 constexpr int kNaGroupM = 8;
 constexpr int kNaMinSplitUnits = 4;
-int noalloc_choose_config(int N) { return N <= 96 ? kNaTallBk24F2 : kNaWideBk32F2Ku16; }
 
 // Once per device, with that device current: symbol address, kernel
 // attributes, occupancy. Called with g_na_mutex held.
@@ -190,7 +187,7 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
   }
 
-  const int id = noalloc_choose_config(N);
+  const int id = choose_config(M, N, K);
   const ConfigEntry& cfg = *kNoAllocConfigs[id];
   const TileShape& S = cfg.shape;
 

@@ -107,6 +107,15 @@ int sgemm_config_info(int id, char* name, int len, int* params);
 int sgemm_force_config(int id);
 
 /*
+ * The configuration sgemm() picks by itself for an M x N x K problem (the
+ * tuned table's entry for the problem's shape class, ignoring
+ * sgemm_force_config). *shape_class (if not NULL) receives the class:
+ * 0 square-large, 1 square-small, 2 K-dominant, 3 N <= 96, 4 M <= 96.
+ * Returns the configuration id or SGEMM_ERR_INVALID_DIM. Host only.
+ */
+int sgemm_choose_config(int M, int N, int K, int* shape_class);
+
+/*
  * The legality checker of the tile configurations, evaluated on the host:
  * 0 if the tuple is legal for the FFMA kernel, else the number of the first
  * rule it breaks. params = {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES,
