@@ -379,6 +379,61 @@ def run_ours(args, w):
     return line
 
 
+REPORT_WORKLOADS = ["square128", "square128_int", "square4096", "edges8191x1000x777",
+                    "kdominant1024x1024x16384", "skinny16384x64x4096"] + \
+    [f"sweep{n}" for n in (256, 512, 1024, 2048, 4096, 8192, 16384)]
+
+
+def run_report(args):
+    """One JSON line per workload: device-timed GFLOP/s of the automatic
+    configuration and its fraction of the FFMA peak (not the default line)."""
+    import torch
+
+    from dense_fp32_gemm_gb300 import binding
+    from dense_fp32_gemm_gb300.workloads import WORKLOADS, make_inputs
+    props = torch.cuda.get_device_properties(0)
+    peaks = measured_peaks()
+    max_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
+    peak_tf = ffma_peak_tflops(props.multi_processor_count, max_mhz)
+    s = torch.cuda.current_stream().cuda_stream
+    for name in REPORT_WORKLOADS:
+        w = WORKLOADS[name]
+        A, B, C = make_inputs(w)
+        dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+
+        def call():
+            st = binding.sgemm(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(),
+                               w.LDB, w.beta, dC.data_ptr(), w.LDC, s)
+            if st != 0:
+                raise RuntimeError(binding.sgemm_status_string(st))
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        reps = max(10, int(200.0 / max(e0.elapsed_time(e1), 1e-3)))
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        st, detail = binding.sgemm_poll_device_status(s)
+        tf = gemm_flops(w.M, w.N, w.K) / ms / 1e9
+        print(json.dumps({"workload": name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                          "beta": w.beta, "ms": round(ms, 5), "gflops": round(tf * 1e3, 1),
+                          "pct_of_ffma_peak": round(100 * tf / peak_tf, 2),
+                          "min_bytes": min_bytes(w.M, w.N, w.K, w.beta),
+                          "achieved_min_gbs": round(min_bytes(w.M, w.N, w.K, w.beta) / ms / 1e6, 1),
+                          "reps": reps, "status": st,
+                          "config": binding.sgemm_last_config()}), flush=True)
+        del dA, dB, dC
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -388,9 +443,14 @@ def main(argv=None):
     ap.add_argument("--workload", default="square4096")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--report", action="store_true",
+                    help="time every named workload and the sweep, one JSON line each")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.report:
+        run_report(args)
+        return
     from dense_fp32_gemm_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)

@@ -131,7 +131,7 @@ def sgemm_force_config(cid: int) -> int:
     return lib().sgemm_force_config(cid)
 
 
-SHAPE_CLASSES = ("square_large", "square_small", "k_dominant", "skinny_n", "skinny_m")
+SHAPE_CLASSES = ("square_large", "square_small", "k_dominant", "skinny_n", "skinny_m", "tiny")
 
 
 def sgemm_choose_config(M, N, K):

@@ -22,6 +22,8 @@ struct KernelParams;
 //          (B arrives by TMA, so a wide BN costs no loader instructions);
 // tall:    256 x 64, 4 warps of 64 x 64, for N <= 64;
 // flat:    64 x 256, 4 warps of 64 x 64, for M <= 64;
+// mini / small: 64 x 64 and 64 x 128 tiles of 2 and 4 warps (8 x 8 per lane)
+//          for problems too small to fill 152 SMs with larger tiles;
 // square:  128 x 128, 4 warps of 64 x 64, two CTAs per SM;
 // pages:   the pages' sweep winner (128 x 64 x 16, warp 64 x 32, WNITER 2,
 //          4 x 4 patches, 128 threads) on this kernel's pipeline;
@@ -45,7 +47,9 @@ struct KernelParams;
   X(SquareBk32F2, 128, 128, 32, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)  \
   X(TallBk24F2, 256, 64, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)     \
   X(WideBk32F2Ku16, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 16, 2) \
-  X(FlatBk24F2, 64, 256, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)
+  X(FlatBk24F2, 64, 256, 24, 64, 64, 2, 4, 4, 128, 3, 2, 8, 2)       \
+  X(MiniF2, 64, 64, 16, 32, 64, 2, 4, 4, 64, 3, 6, 8, 2)              \
+  X(SmallF2, 64, 128, 16, 32, 64, 2, 4, 4, 128, 3, 3, 8, 2)
 
 #define SGEMM_GB300_CFG_STRUCT(NAME, BM, BN, BK, WM, WN, WNI, TM, TN, NT, ST, MINB, KU, OR)     \
   struct Cfg##NAME {                                                                            \

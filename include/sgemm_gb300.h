@@ -110,7 +110,8 @@ int sgemm_force_config(int id);
  * The configuration sgemm() picks by itself for an M x N x K problem (the
  * tuned table's entry for the problem's shape class, ignoring
  * sgemm_force_config). *shape_class (if not NULL) receives the class:
- * 0 square-large, 1 square-small, 2 K-dominant, 3 N <= 96, 4 M <= 96.
+ * 0 square-large, 1 square-small, 2 K-dominant, 3 N <= 96, 4 M <= 96,
+ * 5 tiny (at most 2^28 multiply-adds).
  * Returns the configuration id or SGEMM_ERR_INVALID_DIM. Host only.
  */
 int sgemm_choose_config(int M, int N, int K, int* shape_class);
