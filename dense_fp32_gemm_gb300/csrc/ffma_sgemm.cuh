@@ -387,6 +387,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     const float* b_s = Bs + slot * B_ST + b_frag_off;
     bool next_ok = true;
 
+
     // ---- BK k-steps of outer-product FMA on this slot, KU per chunk ----------
     // One k-step: update the accumulators from fragment buffer `cur`.
     auto kstep = [&](int cur) {
@@ -514,14 +515,40 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
             }
         }
       }
-      // epilogue: C = alpha * acc + beta * C for this lane's RM x RN patch
+      // epilogue: C = alpha * acc + beta * C for this lane's RM x RN patch,
+      // one row group (TM rows x RN columns) at a time: all of the group's
+      // 128-bit reads of C are issued before any of its writes, so their
+      // latencies overlap instead of adding up.
       int tm, tn;
       tile_coords(sc, cpc.tile, tm, tn);
       const int row0 = tm * BM + a_frag_off;
       const int col0 = tn * BN + b_frag_off;
       const float alpha = p.alpha, beta = p.beta;
+      constexpr int QN = WNITER * (TN / 4);  // float4 groups per row
 #pragma unroll
-      for (int wm = 0; wm < WMITER; ++wm)
+      for (int wm = 0; wm < WMITER; ++wm) {
+        float4 old[TM][QN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+          const int row = row0 + wm * WSUBM + i;
+#pragma unroll
+          for (int g = 0; g < QN; ++g) {
+            const int col = col0 + (g / (TN / 4)) * WSUBN + (g % (TN / 4)) * 4;
+            const float* cp = p.C + (long long)row * p.ldc + col;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (beta != 0.f && row < M) {
+              if (p.c_vec && col + 3 < N) {
+                v = *reinterpret_cast<const float4*>(cp);
+              } else {
+                if (col + 0 < N) v.x = cp[0];
+                if (col + 1 < N) v.y = cp[1];
+                if (col + 2 < N) v.z = cp[2];
+                if (col + 3 < N) v.w = cp[3];
+              }
+            }
+            old[i][g] = v;
+          }
+        }
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
           const int row = row0 + wm * WSUBM + i;
@@ -529,36 +556,30 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
           float* crow = p.C + (long long)row * p.ldc;
           const int ai = wm * TM + i;
 #pragma unroll
-          for (int wn = 0; wn < WNITER; ++wn)
-#pragma unroll
-            for (int q = 0; q < TN / 4; ++q) {
-              const int col = col0 + wn * WSUBN + q * 4;
-              const int cj = wn * TN + q * 4;
-              const float r[4] = {SG_ACC(ai, cj), SG_ACC(ai, cj + 1), SG_ACC(ai, cj + 2),
-                                  SG_ACC(ai, cj + 3)};
-              if (p.c_vec && col + 3 < N) {
-                float4 v;
-                if (beta != 0.f) {
-                  const float4 old = *reinterpret_cast<const float4*>(crow + col);
-                  v.x = fmaf(alpha, r[0], beta * old.x);
-                  v.y = fmaf(alpha, r[1], beta * old.y);
-                  v.z = fmaf(alpha, r[2], beta * old.z);
-                  v.w = fmaf(alpha, r[3], beta * old.w);
-                } else {
-                  v = make_float4(alpha * r[0], alpha * r[1], alpha * r[2], alpha * r[3]);
-                }
-                *reinterpret_cast<float4*>(crow + col) = v;
-              } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  if (col + e < N) {
-                    crow[col + e] = beta != 0.f ? fmaf(alpha, r[e], beta * crow[col + e])
-                                                : alpha * r[e];
-                  }
-                }
-              }
+          for (int g = 0; g < QN; ++g) {
+            const int col = col0 + (g / (TN / 4)) * WSUBN + (g % (TN / 4)) * 4;
+            const int cj = (g / (TN / 4)) * TN + (g % (TN / 4)) * 4;
+            float4 v;
+            if (beta != 0.f) {
+              v.x = fmaf(alpha, SG_ACC(ai, cj + 0), beta * old[i][g].x);
+              v.y = fmaf(alpha, SG_ACC(ai, cj + 1), beta * old[i][g].y);
+              v.z = fmaf(alpha, SG_ACC(ai, cj + 2), beta * old[i][g].z);
+              v.w = fmaf(alpha, SG_ACC(ai, cj + 3), beta * old[i][g].w);
+            } else {
+              v = make_float4(alpha * SG_ACC(ai, cj + 0), alpha * SG_ACC(ai, cj + 1),
+                              alpha * SG_ACC(ai, cj + 2), alpha * SG_ACC(ai, cj + 3));
             }
+            if (p.c_vec && col + 3 < N) {
+              *reinterpret_cast<float4*>(crow + col) = v;
+            } else {
+              if (col + 0 < N) crow[col + 0] = v.x;
+              if (col + 1 < N) crow[col + 1] = v.y;
+              if (col + 2 < N) crow[col + 2] = v.z;
+              if (col + 3 < N) crow[col + 3] = v.w;
+            }
+          }
         }
+      }
     }
 #pragma unroll
     for (int i = 0; i < RM / 2; ++i)

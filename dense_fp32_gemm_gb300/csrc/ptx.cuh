@@ -88,6 +88,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Hint: bring the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---- time and inter-CTA flags ---------------------------------------------
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
