@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_set_wait_timeout_ns": (LL, [LL]),
                 "sgemm_noalloc": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_choose_config": (I, [I, I, I, IP]),
+                "sgemm_3xtf32": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -91,6 +92,12 @@ def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
     """Raw call: A, B, C are device addresses (ints), stream a cudaStream_t
     handle (int) or None. Returns the status code."""
     return lib().sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """Opt-in tensor-core path (three TF32 products per FP32 product), same
+    arguments as sgemm(). Returns the status code."""
+    return lib().sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 def sgemm_status_string(status: int) -> str:

@@ -175,6 +175,34 @@ int current_device(int* dev) {
 }
 
 }  // namespace
+
+// ---- internal hooks for the other entry points of the library -------------
+// Scratch of at least `floats` floats (and the status word) in the
+// per-(device, stream) workspace.
+int library_workspace(int dev, cudaStream_t stream, size_t floats, float** scratch, int** status) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  Workspace* ws = nullptr;
+  const int st = get_workspace(dev, stream, 1, floats, &ws);
+  if (st != SGEMM_OK) return st;
+  *scratch = ws->partials;
+  *status = ws->status;
+  return SGEMM_OK;
+}
+
+// SM count of a supported device (and its one-time set-up).
+int library_device_sms(int dev, int* sms) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo* di = nullptr;
+  const int st = device_info(dev, &di);
+  if (st != SGEMM_OK) return st;
+  *sms = di->sms;
+  return SGEMM_OK;
+}
+
+void note_last_config(const char* text) { snprintf(g_last_config, sizeof(g_last_config), "%s", text); }
+
+long long library_wait_timeout_ns() { return g_timeout_ns.load(); }
+
 }  // namespace sgemm_gb300
 
 using namespace sgemm_gb300;

@@ -1,0 +1,101 @@
+// tcgen05.cuh -- inline-PTX wrappers for the 5th-generation tensor cores of
+// sm_100-class parts (tcgen05): tensor-memory allocation, MMA issue and
+// completion, tensor-memory loads, and the shared-memory matrix descriptor.
+#pragma once
+
+#include <stdint.h>
+
+namespace sgemm_gb300 {
+namespace tc {
+
+// ---- tensor memory (TMEM) allocation: one full warp executes these -------
+// Allocates `ncols` columns (a power of two >= 32) of all 128 lanes; the
+// TMEM address is written to shared memory at `dst_smem`.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// ---- ordering of tensor-core work around thread synchronisation ----------
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---- MMA: D[tmem] (+)= A[smem] * B[smem], TF32 inputs, FP32 accumulate ---
+// a_desc / b_desc: shared-memory matrix descriptors; idesc: instruction
+// descriptor; accumulate == 0 overwrites D.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives (once) on the mbarrier when every MMA this thread issued before
+// has completed.
+__device__ __forceinline__ void commit(uint32_t mbar_smem) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          mbar_smem)
+      : "memory");
+}
+
+// ---- TMEM -> registers: 32 lanes x 32 bits, 16 consecutive columns -------
+// Lane i of the warp receives row (lane base + i) of the addressed block.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- shared-memory matrix descriptor ---------------------------------------
+// For a K-major operand tile written by TMA with 128-byte swizzle: rows of
+// 128 bytes (32 TF32 values along K), 8-row swizzle atoms of 1024 bytes laid
+// out one after another along M (or N). Fields: start address >> 4 (bits
+// 0-13), leading byte offset >> 4 (16-29, unused for this layout), stride byte
+// offset >> 4 (32-45: 1024 bytes between 8-row groups), descriptor version 1
+// (46-47), base offset 0 (49-51, the tile is 1024-byte aligned), layout type
+// 2 = 128-byte swizzle (61-63). Moving along K inside the 128-byte row is done
+// by advancing the start address (32 bytes per 8-wide k-step).
+__device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(1u) << 16;                  // leading byte offset (16 B), ignored here
+  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;                    // descriptor version
+  d |= (uint64_t)2u << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::tf32 with FP32 accumulation, both operands
+// K-major: D format F32 (bits 4-5 = 1), A and B format TF32 (bits 7-9 and
+// 10-12 = 2), no negation or transposition, N >> 3 (bits 17-22), M >> 4
+// (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+}  // namespace tc
+}  // namespace sgemm_gb300

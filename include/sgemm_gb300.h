@@ -66,6 +66,20 @@ typedef enum {
 int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
           float beta, float* C, int ldc, void* stream);
 
+/*
+ * Opt-in tensor-core path: the same C = alpha * A * B + beta * C, with the
+ * same arguments, checks and workspace, computed as three TF32 products per
+ * FP32 product on the tcgen05 tensor cores (each operand split into a TF32
+ * high part and a TF32 residual; the dropped residual product is below
+ * 3 * 2^-20 of sum |a||b|, inside the library's FP32 tolerance, and integer
+ * inputs up to 2^11 stay exact). The pages have no tensor-core kernel; this is
+ * the split-operand method of Ootomo and Yokota (2022). It uses 8 * (M + N) *
+ * K bytes of workspace for the split operands. Reported separately from the
+ * FFMA path.
+ */
+int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                 int ldb, float beta, float* C, int ldc, void* stream);
+
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* sgemm_status_string(int status);
 

@@ -32,10 +32,13 @@ def device_buffer(host_flat: torch.Tensor, offset_floats: int = 0):
     return store, view
 
 
-def run_cuda(w: Workload, A, B, C, offsets=(0, 0, 0), config=None, stream=None, check_status=True):
+def run_cuda(w: Workload, A, B, C, offsets=(0, 0, 0), config=None, stream=None, check_status=True,
+             fn=None):
     """Run the CUDA path on host inputs (flat float32 tensors with the
     workload's leading dimensions) and return the device result copied back as
-    a flat numpy array (M*ldc floats)."""
+    a flat numpy array (M*ldc floats). `fn` is the C-ABI entry point
+    (default: sgemm; sgemm_3xtf32 for the tensor-core path)."""
+    fn = fn or binding.sgemm
     _, dA = device_buffer(A, offsets[0])
     _, dB = device_buffer(B, offsets[1])
     if C is None:
@@ -45,8 +48,8 @@ def run_cuda(w: Workload, A, B, C, offsets=(0, 0, 0), config=None, stream=None, 
         assert binding.sgemm_force_config(config) == 0
     try:
         s = stream if stream is not None else torch.cuda.current_stream()
-        st = binding.sgemm(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(), w.LDB,
-                           w.beta, dC.data_ptr(), w.LDC, s.cuda_stream)
+        st = fn(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(), w.LDB,
+                w.beta, dC.data_ptr(), w.LDC, s.cuda_stream)
         assert st == 0, f"sgemm returned {st}: {binding.sgemm_status_string(st)}"
         if check_status:
             pst, detail = binding.sgemm_poll_device_status(s.cuda_stream)
@@ -85,10 +88,10 @@ def assert_match(w: Workload, gpu2d: np.ndarray, ref: np.ndarray, mag: np.ndarra
             f"first at ({i},{j}): gpu={g[i, j]!r} ref={ref[i, j]!r} mag={mag[i, j]!r}")
 
 
-def check_against_oracle(w: Workload, offsets=(0, 0, 0), config=None, pad=float("nan")):
+def check_against_oracle(w: Workload, offsets=(0, 0, 0), config=None, pad=float("nan"), fn=None):
     """Whole-result comparison (sizes the oracle finishes in seconds)."""
     A, B, C = make_inputs(w, pad_value=pad)
-    out = run_cuda(w, A, B, C, offsets=offsets, config=config)
+    out = run_cuda(w, A, B, C, offsets=offsets, config=config, fn=fn)
     ref, mag = oracle_full(w, A, B, C)
     gpu = logical(out, w.M, w.N, w.LDC)
     assert_match(w, gpu, ref, mag, what=f"config={config} offsets={offsets}")
@@ -100,12 +103,12 @@ def check_against_oracle(w: Workload, offsets=(0, 0, 0), config=None, pad=float(
     return gpu
 
 
-def check_sampled(w: Workload, rows=32, elements=2048, config=None):
+def check_sampled(w: Workload, rows=32, elements=2048, config=None, fn=None):
     """Large sizes: oracle on sampled full rows and random elements; for
     integer inputs also a Freivalds check of every element,
     C x == alpha A (B x) + beta C_in x, exact in float64."""
     A, B, C = make_inputs(w)
-    out = run_cuda(w, A, B, C, config=config)
+    out = run_cuda(w, A, B, C, config=config, fn=fn)
     gpu = logical(out, w.M, w.N, w.LDC)
     Cn = None if w.beta == 0 else C.numpy()
     r = row_sample(w.M, rows, w.seed)

@@ -1,0 +1,74 @@
+"""The opt-in tensor-core path (sgemm_3xtf32) against the oracle: the same
+bar as the FFMA path -- bit-exact on integer inputs, the FP32 tolerance
+|C - C_ref| <= 1e-5 * (|alpha| sum |a||b| + |beta| |c|) + 1e-30 on real inputs --
+on small shapes element by element and on the full workloads by sampling."""
+import numpy as np
+import pytest
+import torch
+
+from dense_fp32_gemm_gb300 import binding
+from dense_fp32_gemm_gb300.workloads import SWEEP_SIZES, WORKLOADS, Workload, integer_variant, make_inputs
+
+import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+X3 = binding.sgemm_3xtf32
+
+SHAPES = [(128, 256, 32), (1, 1, 1), (7, 9, 3), (33, 65, 17), (257, 129, 100), (300, 520, 77),
+          (129, 257, 1000), (513, 1031, 40), (64, 64, 4097), (2, 700, 2049), (1000, 40, 129)]
+
+
+@pytest.mark.parametrize("dist", ["int3", "uniform", "normal"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_shapes(shape, dist):
+    M, N, K = shape
+    H.check_against_oracle(Workload("x3", M, N, K, 1.25, -0.5, dist, 31), fn=X3)
+
+
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
+def test_unaligned_and_padded(offsets):
+    w = Workload("x3pad", 301, 203, 777, 1.25, -0.5, "normal", 32, lda=779, ldb=207, ldc=210)
+    H.check_against_oracle(w, offsets=offsets, fn=X3)
+    H.check_against_oracle(w.with_(dist="int3"), offsets=offsets, fn=X3)
+
+
+def test_beta_zero_does_not_read_c():
+    w = Workload("x3beta0", 140, 300, 50, 1.0, 0.0, "uniform", 33)
+    A, B, _ = make_inputs(w)
+    out = H.run_cuda(w, A, B, torch.full((w.M * w.LDC,), float("nan")), fn=X3)
+    ref, mag = H.oracle_full(w, A, B, None)
+    H.assert_match(w, H.logical(out, w.M, w.N, w.LDC), ref, mag)
+
+
+def test_alpha_zero_scales_c():
+    w = Workload("x3alpha0", 70, 90, 33, 0.0, -0.5, "int3", 34)
+    _, _, C = make_inputs(w)
+    out = H.run_cuda(w, torch.full((w.M * w.LDA,), float("nan")),
+                     torch.full((w.K * w.LDB,), float("nan")), C, fn=X3)
+    assert np.array_equal(H.logical(out, w.M, w.N, w.LDC).astype(np.float64),
+                          -0.5 * C.numpy().astype(np.float64).reshape(w.M, w.N))
+
+
+def test_repeat_calls_are_bitwise_deterministic():
+    w = Workload("x3det", 300, 700, 3000, 1.0, 0.0, "uniform", 35)
+    A, B, C = make_inputs(w)
+    first = H.run_cuda(w, A, B, C, fn=X3)
+    assert np.array_equal(first, H.run_cuda(w, A, B, C, fn=X3))
+
+
+NAMED = ["square4096", "edges8191x1000x777", "kdominant1024x1024x16384", "skinny16384x64x4096"]
+
+
+@pytest.mark.parametrize("name", NAMED)
+def test_named_real(name):
+    H.check_sampled(WORKLOADS[name], rows=8, elements=1024, fn=X3)
+
+
+@pytest.mark.parametrize("name", NAMED)
+def test_named_integer_bit_exact(name):
+    H.check_sampled(integer_variant(WORKLOADS[name]), rows=4, elements=512, fn=X3)
+
+
+@pytest.mark.parametrize("n", [s for s in SWEEP_SIZES if s <= 8192])
+def test_sweep_integer_bit_exact(n):
+    H.check_sampled(WORKLOADS[f"sweep{n}_int"], rows=4, elements=512, fn=X3)
