@@ -65,6 +65,17 @@ def ffma_peak_tflops(sms, mhz):
     return sms * mhz * 1e6 * FFMA_FLOP_PER_CLK_PER_SM / 1e12
 
 
+# Nominal dense tensor rates of GB300 (TF32 1.1 PF/s, BF16 2.25 PF/s): the
+# TF32 peak is the measured BF16 cuBLAS peak times their ratio. The 3xTF32 path
+# issues three TF32 products per FP32 product, so its useful-FLOP roof is a third.
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def tf32x3_peak_tflops(peaks):
+    bf16 = peaks.get("bf16_tflops")
+    return (float(bf16) * TF32_OVER_BF16 / 3.0) if bf16 else None
+
+
 def kernel_source_hash():
     """Hash of the sources that define the GEMM kernels (the C-ABI file,
     which only validates and dispatches, is left out)."""
@@ -323,6 +334,34 @@ def run_ours(args, w):
     total_max = max_over_ranks(total_s, world)
     value = aggregate(gemm_flops(w.M, w.N, w.K), args.steps, total_max, world)
 
+    # ---- the opt-in tensor-core path on the same workload (reported apart) ---------
+    tf32x3 = None
+    if args.tf32x3:
+        def step3():
+            st3 = binding.sgemm_3xtf32(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA,
+                                       dB.data_ptr(), w.LDB, w.beta, dC.data_ptr(), w.LDC, sh)
+            if st3 != 0:
+                raise RuntimeError(f"sgemm_3xtf32: {binding.sgemm_status_string(st3)}")
+        for _ in range(args.warmup):
+            step3()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for _ in range(args.steps):
+            step3()
+        e3.record(stream)
+        torch.cuda.synchronize(dev)
+        t3 = max_over_ranks(s3.elapsed_time(e3) / 1e3, world)
+        st, detail = binding.sgemm_poll_device_status(sh)
+        if st != 0:
+            raise RuntimeError(f"device status {st} detail {detail} after the 3xTF32 steps")
+        v3 = aggregate(gemm_flops(w.M, w.N, w.K), args.steps, t3, world)
+        tf32x3 = {"value": round(v3, 1), "unit": UNIT, "ms_per_step": round(t3 / args.steps * 1e3, 4),
+                  "config": binding.sgemm_last_config(),
+                  "note": "opt-in sgemm_3xtf32: split-operand TF32 on tcgen05, same FP32 tolerance; "
+                          "includes its split pre-pass kernels"}
+
     # ---- end to end from pinned host buffers --------------------------------------
     e2e_steps = max(3, min(args.steps, 20))
     hA, hB, hC = A.pin_memory(), B.pin_memory(), C.pin_memory()
@@ -374,6 +413,15 @@ def run_ours(args, w):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if tf32x3 is not None:
+        p3 = tf32x3_peak_tflops(peaks)
+        a3 = tf32x3["value"] / 1e3
+        tf32x3["roofline"] = {"bound": "tensor", "achieved": round(a3, 3),
+                              "peak": round(p3, 3) if p3 else None, "unit": "TFLOP/s",
+                              "frac": round(a3 / p3, 4) if p3 else None,
+                              "peak_basis": "measured bf16 peak x 1.1/2.25 (TF32/BF16 nominal) / 3 "
+                                            "TF32 products per FP32 product"}
+        line["tf32x3"] = tf32x3
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, C, budget_s=args.cpu_budget)
     return line
@@ -423,12 +471,37 @@ def run_report(args):
         ms = e0.elapsed_time(e1) / reps
         st, detail = binding.sgemm_poll_device_status(s)
         tf = gemm_flops(w.M, w.N, w.K) / ms / 1e9
-        print(json.dumps({"workload": name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
-                          "beta": w.beta, "ms": round(ms, 5), "gflops": round(tf * 1e3, 1),
+        print(json.dumps({"workload": name, "path": "ffma", "M": w.M, "N": w.N, "K": w.K,
+                          "alpha": w.alpha, "beta": w.beta, "ms": round(ms, 5),
+                          "gflops": round(tf * 1e3, 1),
                           "pct_of_ffma_peak": round(100 * tf / peak_tf, 2),
                           "min_bytes": min_bytes(w.M, w.N, w.K, w.beta),
                           "achieved_min_gbs": round(min_bytes(w.M, w.N, w.K, w.beta) / ms / 1e6, 1),
                           "reps": reps, "status": st,
+                          "config": binding.sgemm_last_config()}), flush=True)
+        # the opt-in tensor-core path, reported apart
+        def call3():
+            st3 = binding.sgemm_3xtf32(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA,
+                                       dB.data_ptr(), w.LDB, w.beta, dC.data_ptr(), w.LDC, s)
+            if st3 != 0:
+                raise RuntimeError(binding.sgemm_status_string(st3))
+        for _ in range(3):
+            call3()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            call3()
+        e1.record()
+        torch.cuda.synchronize()
+        ms3 = e0.elapsed_time(e1) / reps
+        st3, _ = binding.sgemm_poll_device_status(s)
+        tf3 = gemm_flops(w.M, w.N, w.K) / ms3 / 1e9
+        p3 = tf32x3_peak_tflops(peaks)
+        print(json.dumps({"workload": name, "path": "3xtf32", "M": w.M, "N": w.N, "K": w.K,
+                          "alpha": w.alpha, "beta": w.beta, "ms": round(ms3, 5),
+                          "gflops": round(tf3 * 1e3, 1),
+                          "pct_of_3xtf32_tensor_roof": round(100 * tf3 / p3, 2) if p3 else None,
+                          "reps": reps, "status": st3,
                           "config": binding.sgemm_last_config()}), flush=True)
         del dA, dB, dC
         torch.cuda.empty_cache()
@@ -443,6 +516,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="square4096")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-tf32x3", dest="tf32x3", action="store_false",
+                    help="skip timing the opt-in 3xTF32 tensor-core path")
     ap.add_argument("--report", action="store_true",
                     help="time every named workload and the sweep, one JSON line each")
     args = ap.parse_args(argv)

@@ -179,13 +179,21 @@ int current_device(int* dev) {
 // ---- internal hooks for the other entry points of the library -------------
 // Scratch of at least `floats` floats (and the status word) in the
 // per-(device, stream) workspace.
-int library_workspace(int dev, cudaStream_t stream, size_t floats, float** scratch, int** status) {
+// With nflags > 0 it also returns the flag array and this call's epoch (a
+// value no flag holds before this call publishes it).
+int library_workspace(int dev, cudaStream_t stream, size_t floats, size_t nflags, float** scratch,
+                      int** status, uint32_t** flags, uint32_t* epoch) {
   std::lock_guard<std::mutex> lock(g_mutex);
   Workspace* ws = nullptr;
-  const int st = get_workspace(dev, stream, 1, floats, &ws);
+  const int st = get_workspace(dev, stream, nflags > 0 ? nflags : 1, floats, &ws);
   if (st != SGEMM_OK) return st;
   *scratch = ws->partials;
   *status = ws->status;
+  if (flags != nullptr) *flags = ws->flags;
+  if (epoch != nullptr) {
+    if (++ws->epoch == 0) ws->epoch = 1;
+    *epoch = ws->epoch;
+  }
   return SGEMM_OK;
 }
 

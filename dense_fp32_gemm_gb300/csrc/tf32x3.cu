@@ -44,7 +44,8 @@
 namespace sgemm_gb300 {
 
 // Provided by api.cu.
-int library_workspace(int dev, cudaStream_t stream, size_t floats, float** scratch, int** status);
+int library_workspace(int dev, cudaStream_t stream, size_t floats, size_t nflags, float** scratch,
+                      int** status, uint32_t** flags, uint32_t* epoch);
 int library_device_sms(int dev, int* sms);
 void note_last_config(const char* text);
 long long library_wait_timeout_ns();
@@ -55,16 +56,19 @@ constexpr int BM = 128, BN = 256, BK = 32, ST = 2, NT = 192;
 constexpr int A_BYTES = BM * BK * 4;                      // 16 KB
 constexpr int B_BYTES = BN * BK * 4;                      // 32 KB
 constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 KB
-constexpr int TMEM_COLS = 256;
+constexpr int ACC_COLS = BN;              // one FP32 accumulator: 128 lanes x BN columns
+constexpr int TMEM_COLS = 2 * ACC_COLS;   // two, so the epilogue overlaps the next MMAs
+constexpr int EPI_THREADS = 128;          // warps 2-5
 constexpr uint32_t IDESC = tc::idesc_tf32(BM, BN);
 static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
 
 struct Barriers {
-  uint64_t full[ST];     // TMA transaction bytes of one stage
-  uint64_t empty[ST];    // MMAs that read a stage have completed
-  uint64_t tmem_full;    // the tile's last MMA has completed
-  uint64_t tmem_empty;   // the epilogue warps have read the accumulator
-  uint64_t drain;        // final MMA completion on the abort path
+  uint64_t full[ST];       // TMA transaction bytes of one stage
+  uint64_t empty[ST];      // MMAs that read a stage have completed
+  uint64_t tmem_full[2];   // a piece's last MMA into accumulator i has completed
+  uint64_t tmem_empty[2];  // the epilogue warps have read accumulator i
+  uint64_t drain;          // final MMA completion on the abort path
+  uint64_t epi_sync;       // rendezvous of the 128 epilogue threads
   uint32_t tmem_addr;
   int abort;
 };
@@ -75,7 +79,10 @@ struct Params {
   float alpha, beta;
   float* C;
   long long ldc;
-  Schedule sched;   // tile numbering (whole tiles only, round-robin)
+  Schedule sched;     // whole tiles, then K-split tiles (schedule.hpp)
+  float* ws;          // grid partial tiles of BM x BN floats, column-major
+  uint32_t* flags;    // flags[b] == epoch once CTA b's partial is written
+  uint32_t epoch;
   int* status;
   long long timeout_ns;
 };
@@ -84,17 +91,36 @@ __device__ __forceinline__ float tf32_trunc(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
-// A (M x K, lda) -> A_hi, A_lo (M x K, ldw).
+// A (M x K, lda) -> A_hi, A_lo (M x K, ldw). Rows over blockIdx.y (strided
+// by gridDim.y), groups of 4 columns over x; 128-bit loads and stores when
+// the row starts of A are 16-byte aligned (ldw is a multiple of 4).
 __global__ void split_a_kernel(int M, int K, const float* __restrict__ A, long long lda,
-                               float* __restrict__ hi, float* __restrict__ lo, long long ldw) {
-  const long long total = (long long)M * K;
-  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-       e += (long long)gridDim.x * blockDim.x) {
-    const long long m = e / K, k = e % K;
-    const float x = A[m * lda + k];
-    const float h = tf32_trunc(x);
-    hi[m * ldw + k] = h;
-    lo[m * ldw + k] = tf32_trunc(x - h);
+                               float* __restrict__ hi, float* __restrict__ lo, long long ldw,
+                               int vec) {
+  const int groups = (K + 3) / 4;
+  for (int m = blockIdx.y; m < M; m += gridDim.y) {
+    const float* a = A + (long long)m * lda;
+    float* h = hi + (long long)m * ldw;
+    float* l = lo + (long long)m * ldw;
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += gridDim.x * blockDim.x) {
+      const int k = g * 4;
+      if (vec && k + 3 < K) {
+        const float4 x = *reinterpret_cast<const float4*>(a + k);
+        const float4 xh = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z),
+                                      tf32_trunc(x.w));
+        *reinterpret_cast<float4*>(h + k) = xh;
+        *reinterpret_cast<float4*>(l + k) =
+            make_float4(tf32_trunc(x.x - xh.x), tf32_trunc(x.y - xh.y), tf32_trunc(x.z - xh.z),
+                        tf32_trunc(x.w - xh.w));
+      } else {
+        for (int e = 0; e < 4 && k + e < K; ++e) {
+          const float x = a[k + e];
+          const float xh = tf32_trunc(x);
+          h[k + e] = xh;
+          l[k + e] = tf32_trunc(x - xh);
+        }
+      }
+    }
   }
 }
 
@@ -144,16 +170,20 @@ __global__ void __launch_bounds__(NT, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Schedule& sc = p.sched;
-  const int kiters = sc.kiters;
+  const int b = blockIdx.x;
+  const int npieces = num_pieces(sc, b);
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bar->full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), 1);
     }
-    ptx::mbar_init(ptx::smem_addr(&bar->tmem_full), 1);
-    ptx::mbar_init(ptx::smem_addr(&bar->tmem_empty), 4);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&bar->tmem_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bar->tmem_empty[i]), 4);
+    }
     ptx::mbar_init(ptx::smem_addr(&bar->drain), 1);
+    ptx::mbar_init(ptx::smem_addr(&bar->epi_sync), EPI_THREADS);
     bar->abort = 0;
     ptx::mbar_fence_init();
     ptx::tma_prefetch_desc(&tmA_hi);
@@ -171,18 +201,22 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tmem = bar->tmem_addr;
 
   if (warp == 0) {
-    // ---- TMA producer ---------------------------------------------------------
+    // ---- TMA producer: the four operand tiles of every k-slice of every piece
     if (lane == 0) {
       int it = 0;
-      for (int t = blockIdx.x; t < sc.tiles && !*abort_w; t += gridDim.x) {
+      for (int i = 0; i < npieces && !*abort_w; ++i) {
+        const Piece pc = get_piece(sc, b, i);
         int tm, tn;
-        tile_coords(sc, t, tm, tn);
-        for (int kb = 0; kb < kiters; ++kb, ++it) {
+        tile_coords(sc, pc.tile, tm, tn);
+        bool ok = true;
+        for (int kb = pc.kb; kb < pc.ke; ++kb, ++it) {
           const int s = it % ST;
           const uint32_t par = (uint32_t)((it / ST) & 1) ^ 1u;
           if (!bounded_wait(ptx::smem_addr(&bar->empty[s]), par, abort_w, p.status,
-                            kDevTimeoutEmpty, p.timeout_ns))
+                            kDevTimeoutEmpty, p.timeout_ns)) {
+            ok = false;
             break;
+          }
           const uint32_t fb = ptx::smem_addr(&bar->full[s]);
           const uint32_t st0 = base_addr + (uint32_t)(s * STAGE_BYTES);
           ptx::mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
@@ -191,6 +225,7 @@ __global__ void __launch_bounds__(NT, 1)
           ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB_hi, kb * BK, tn * BN, fb);
           ptx::tma_load_2d(st0 + 2 * A_BYTES + B_BYTES, &tmB_lo, kb * BK, tn * BN, fb);
         }
+        if (!ok) break;
       }
       // nothing may land after the CTA is gone: wait (bounded) for the last
       // stages issued
@@ -202,18 +237,21 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer -----------------------------------------------------------
+    // ---- MMA issuer: piece i accumulates into TMEM columns (i % 2) * BN ------
     if (lane == 0) {
-      int it = 0, tcount = 0;
+      int it = 0;
       bool issued_any = false;
-      for (int t = blockIdx.x; t < sc.tiles && !*abort_w; t += gridDim.x, ++tcount) {
-        // the epilogue must have read the previous tile's accumulator
-        if (!bounded_wait(ptx::smem_addr(&bar->tmem_empty), (uint32_t)(tcount & 1) ^ 1u, abort_w,
-                          p.status, kDevTimeoutSync, p.timeout_ns))
+      for (int i = 0; i < npieces && !*abort_w; ++i) {
+        const Piece pc = get_piece(sc, b, i);
+        const int buf = i & 1;
+        const uint32_t d = tmem + (uint32_t)(buf * ACC_COLS);
+        // the epilogue must have read this accumulator's previous piece
+        if (!bounded_wait(ptx::smem_addr(&bar->tmem_empty[buf]), (uint32_t)((i >> 1) & 1) ^ 1u,
+                          abort_w, p.status, kDevTimeoutSync, p.timeout_ns))
           break;
         tc::fence_after_sync();
         bool ok = true;
-        for (int kb = 0; kb < kiters; ++kb, ++it) {
+        for (int kb = pc.kb; kb < pc.ke; ++kb, ++it) {
           const int s = it % ST;
           if (!bounded_wait(ptx::smem_addr(&bar->full[s]), (uint32_t)((it / ST) & 1), abort_w,
                             p.status, kDevTimeoutFull, p.timeout_ns)) {
@@ -229,16 +267,16 @@ __global__ void __launch_bounds__(NT, 1)
             const uint64_t a_lo = tc::smem_desc_k_sw128(st0 + A_BYTES + koff);
             const uint64_t b_hi = tc::smem_desc_k_sw128(st0 + 2 * A_BYTES + koff);
             const uint64_t b_lo = tc::smem_desc_k_sw128(st0 + 2 * A_BYTES + B_BYTES + koff);
-            const uint32_t first = (kb == 0 && kk == 0) ? 0u : 1u;
-            tc::mma_tf32(tmem, a_hi, b_hi, IDESC, first);
-            tc::mma_tf32(tmem, a_hi, b_lo, IDESC, 1u);
-            tc::mma_tf32(tmem, a_lo, b_hi, IDESC, 1u);
+            const uint32_t first = (kb == pc.kb && kk == 0) ? 0u : 1u;
+            tc::mma_tf32(d, a_hi, b_hi, IDESC, first);
+            tc::mma_tf32(d, a_hi, b_lo, IDESC, 1u);
+            tc::mma_tf32(d, a_lo, b_hi, IDESC, 1u);
           }
           issued_any = true;
           tc::commit(ptx::smem_addr(&bar->empty[s]));  // frees the stage when done
         }
         if (!ok) break;
-        tc::commit(ptx::smem_addr(&bar->tmem_full));  // the tile's accumulator is ready
+        tc::commit(ptx::smem_addr(&bar->tmem_full[buf]));  // the piece's accumulator is ready
       }
       if (*abort_w && issued_any) {
         // wait (bounded) until every MMA issued has completed
@@ -249,55 +287,112 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   } else {
-    // ---- epilogue warps 2-5: TMEM -> registers -> C ---------------------------
+    // ---- epilogue warps 2-5: TMEM -> registers -> C, or -> a partial tile ----
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;            // this thread's row of the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    int tcount = 0;
-    for (int t = blockIdx.x; t < sc.tiles && !*abort_w; t += gridDim.x, ++tcount) {
-      const bool ok = bounded_wait(ptx::smem_addr(&bar->tmem_full), (uint32_t)(tcount & 1),
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) && ((p.ldc & 3) == 0);
+    uint32_t sync_phase = 0;
+    auto epi_sync = [&]() -> bool {  // bounded rendezvous of the 128 epilogue threads
+      ptx::mbar_arrive(ptx::smem_addr(&bar->epi_sync));
+      const bool ok = bounded_wait(ptx::smem_addr(&bar->epi_sync), sync_phase, abort_w, p.status,
+                                   kDevTimeoutSync, p.timeout_ns);
+      sync_phase ^= 1u;
+      return __all_sync(0xffffffffu, ok);
+    };
+    for (int i = 0; i < npieces && !*abort_w; ++i) {
+      const Piece pc = get_piece(sc, b, i);
+      const int buf = i & 1;
+      const uint32_t acc = tmem + (uint32_t)(buf * ACC_COLS) + lane_base;
+      const bool ok = bounded_wait(ptx::smem_addr(&bar->tmem_full[buf]), (uint32_t)((i >> 1) & 1),
                                    abort_w, p.status, kDevTimeoutFull, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after_sync();
-      int tm, tn;
-      tile_coords(sc, t, tm, tn);
-      const int row = tm * BM + quarter * 32 + lane;
-      const bool row_ok = row < p.M;
-      float* crow = p.C + (long long)(row_ok ? row : 0) * p.ldc;
-      const bool vec = ((reinterpret_cast<uintptr_t>(p.C) & 15u) == 0) && ((p.ldc & 3) == 0);
+      float* my_ws = p.ws + (long long)b * (BM * BN);
+      if (is_partial_piece(sc, pc)) {
+        // publish the partial tile (column-major: a warp writes 128 bytes
+        // per column)
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + lane_base + (uint32_t)c0, r);
-        tc::tmem_wait_ld();
-        if (!row_ok) continue;
-        const int col0 = tn * BN + c0;
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t v[16];
+          tc::tmem_ld16(acc + (uint32_t)c0, v);
+          tc::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = col0 + q * 4;
-          float v[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r[q * 4 + e]);
-          if (vec && col + 3 < p.N) {
-            float4 o = make_float4(v[0], v[1], v[2], v[3]);
-            if (p.beta != 0.f) {
-              const float4 c = *reinterpret_cast<const float4*>(crow + col);
-              o.x = fmaf(p.beta, c.x, v[0]);
-              o.y = fmaf(p.beta, c.y, v[1]);
-              o.z = fmaf(p.beta, c.z, v[2]);
-              o.w = fmaf(p.beta, c.w, v[3]);
+          for (int e = 0; e < 16; ++e) __stcg(my_ws + (c0 + e) * BM + r, __uint_as_float(v[e]));
+        }
+        if (!epi_sync()) break;
+        if (warp == 2 && lane == 0) {
+          __threadfence();
+          ptx::st_release(p.flags + b, p.epoch);
+        }
+      } else {
+        const int nc = num_contributors(sc, b, pc);
+        if (nc > 0) {
+          if (warp == 2 && lane == 0) {
+            for (int c = 1; c <= nc && !*abort_w; ++c) {
+              const uint32_t* f = p.flags + b + c;
+              const uint64_t t0 = ptx::global_ns();
+              while (ptx::ld_acquire(f) != p.epoch) {
+                if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) {
+                  *abort_w = 1;
+                  atomicCAS(p.status, 0, (int)kDevTimeoutFlag);
+                  break;
+                }
+                __nanosleep(200);
+              }
             }
-            *reinterpret_cast<float4*>(crow + col) = o;
-          } else {
+          }
+          if (!epi_sync() || *abort_w) break;
+        }
+        int tm, tn;
+        tile_coords(sc, pc.tile, tm, tn);
+        const int row = tm * BM + r;
+        const bool row_ok = row < p.M;
+        float* crow = p.C + (long long)(row_ok ? row : 0) * p.ldc;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t v[16];
+          tc::tmem_ld16(acc + (uint32_t)c0, v);
+          tc::tmem_wait_ld();
+          float a[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (col + e < p.N)
-                crow[col + e] = p.beta != 0.f ? fmaf(p.beta, crow[col + e], v[e]) : v[e];
+          for (int e = 0; e < 16; ++e) a[e] = __uint_as_float(v[e]);
+          // partials of CTAs b+1 .. b+nc, in that order
+          for (int c = 1; c <= nc; ++c) {
+            const float* src = my_ws + (long long)c * (BM * BN);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) a[e] += __ldcg(src + (c0 + e) * BM + r);
+          }
+          if (!row_ok) continue;
+          const int col0 = tn * BN + c0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int col = col0 + q * 4;
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = p.alpha * a[q * 4 + e];
+            if (vec && col + 3 < p.N) {
+              float4 w4 = make_float4(o[0], o[1], o[2], o[3]);
+              if (p.beta != 0.f) {
+                const float4 c = *reinterpret_cast<const float4*>(crow + col);
+                w4.x = fmaf(p.beta, c.x, o[0]);
+                w4.y = fmaf(p.beta, c.y, o[1]);
+                w4.z = fmaf(p.beta, c.z, o[2]);
+                w4.w = fmaf(p.beta, c.w, o[3]);
+              }
+              *reinterpret_cast<float4*>(crow + col) = w4;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (col + e < p.N)
+                  crow[col + e] = p.beta != 0.f ? fmaf(p.beta, crow[col + e], o[e]) : o[e];
+            }
           }
         }
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bar->tmem_empty));
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bar->tmem_empty[buf]));
     }
   }
 
@@ -393,24 +488,37 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   }
   if (enc == nullptr) return SGEMM_ERR_LAUNCH;
 
-  // workspace: A_hi, A_lo (M x Kp) and B_hi, B_lo transposed (N x Kp)
+  // schedule: whole tiles, then the last one to two waves split along K
+  const int tiles_m = (M + x3::BM - 1) / x3::BM, tiles_n = (N + x3::BN - 1) / x3::BN;
+  const int kiters = (K + x3::BK - 1) / x3::BK;
+  const Schedule sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, 2);
+  const bool split = sched.dp_tiles < sched.tiles;
+
+  // workspace: A_hi, A_lo (M x Kp), B_hi, B_lo transposed (N x Kp), then one
+  // partial tile per CTA when the schedule splits
   const long long Kp = ((long long)K + 3) / 4 * 4;
-  const size_t floats = (size_t)(2 * (long long)M * Kp + 2 * (long long)N * Kp);
+  const size_t split_floats = (size_t)(2 * (long long)M * Kp + 2 * (long long)N * Kp);
+  const size_t partial_floats = split ? (size_t)sched.grid * x3::BM * x3::BN : 0;
   float* ws = nullptr;
   int* status = nullptr;
-  st = library_workspace(dev, stream, floats, &ws, &status);
+  uint32_t* flags = nullptr;
+  uint32_t epoch = 0;
+  st = library_workspace(dev, stream, split_floats + partial_floats, (size_t)sched.grid, &ws, &status,
+                         &flags, &epoch);
   if (st != SGEMM_OK) return st;
   float* a_hi = ws;
   float* a_lo = a_hi + (size_t)M * Kp;
   float* b_hi = a_lo + (size_t)M * Kp;
   float* b_lo = b_hi + (size_t)N * Kp;
+  float* partials = b_lo + (size_t)N * Kp;
 
   // 1. split (and transpose B)
   {
-    const long long total = (long long)M * K;
-    int blocks = (int)((total + 255) / 256);
-    if (blocks > sms * 16) blocks = sms * 16;
-    x3::split_a_kernel<<<blocks, 256, 0, stream>>>(M, K, A, lda, a_hi, a_lo, Kp);
+    const int groups = (K + 3) / 4;
+    const int bx = (groups + 127) / 128 < 8 ? (groups + 127) / 128 : 8;
+    const int by = M < 65535 ? M : 65535;
+    const int vec = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0);
+    x3::split_a_kernel<<<dim3(bx, by), 128, 0, stream>>>(M, K, A, lda, a_hi, a_lo, Kp, vec);
     dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
     x3::split_bt_kernel<<<grid, block, 0, stream>>>(K, N, B, ldb, b_hi, b_lo, Kp);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -431,17 +539,18 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   p.beta = beta;
   p.C = C;
   p.ldc = ldc;
-  const int tiles_m = (M + x3::BM - 1) / x3::BM, tiles_n = (N + x3::BN - 1) / x3::BN;
-  const int kiters = (K + x3::BK - 1) / x3::BK;
-  // whole tiles only (a minimum split of 2^20 k-slices disables the split)
-  p.sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, 1 << 20);
+  p.sched = sched;
+  p.ws = partials;
+  p.flags = flags;
+  p.epoch = epoch;
   p.status = status;
   p.timeout_ns = library_wait_timeout_ns();
   x3::gemm_kernel<<<p.sched.grid, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi, mB_lo);
   if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
   char text[160];
-  snprintf(text, sizeof(text), "3xtf32_tcgen05_%dx%dx%d_s%d grid=%d tiles=%d kiters=%d", x3::BM,
-           x3::BN, x3::BK, x3::ST, p.sched.grid, p.sched.tiles, kiters);
+  snprintf(text, sizeof(text), "3xtf32_tcgen05_%dx%dx%d_s%d grid=%d dp=%d split=%d kiters=%d",
+           x3::BM, x3::BN, x3::BK, x3::ST, sched.grid, sched.dp_tiles,
+           sched.tiles - sched.dp_tiles, kiters);
   note_last_config(text);
   return SGEMM_OK;
 }
