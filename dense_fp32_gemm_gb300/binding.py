@@ -27,6 +27,9 @@ SGEMM_ERR_MISALIGNED = -8
 SGEMM_ERR_INVALID_VALUE = -9
 SGEMM_ERR_NOALLOC_CAPACITY = -10
 
+SGEMM_OP_N = 0
+SGEMM_OP_T = 1
+
 PARAM_NAMES = ("BM", "BN", "BK", "WM", "WN", "WNITER", "TM", "TN", "NT", "STAGES", "MINB", "KU", "ORDER")
 
 
@@ -70,6 +73,9 @@ def lib() -> ctypes.CDLL:
                 "sgemm_noalloc": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_choose_config": (I, [I, I, I, IP]),
                 "sgemm_3xtf32": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_ex": (I, [I, I, I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
+                                              I, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -92,6 +98,18 @@ def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
     """Raw call: A, B, C are device addresses (ints), stream a cudaStream_t
     handle (int) or None. Returns the status code."""
     return lib().sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_ex(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """C = alpha*op(A)*op(B) + beta*C (ops SGEMM_OP_N / SGEMM_OP_T)."""
+    return lib().sgemm_ex(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_strided_batched(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C,
+                          ldc, strideC, batch, stream=None) -> int:
+    """`batch` products C_i = alpha*op(A_i)*op(B_i) + beta*C_i, one launch."""
+    return lib().sgemm_strided_batched(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                                       beta, C, ldc, strideC, batch, stream)
 
 
 def sgemm_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

@@ -46,7 +46,7 @@ struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int sms = 0;
-  int occupancy[kNumConfigs][2] = {};  // [config][tma]
+  int occupancy[kNumConfigs] = {};  // resident CTAs per SM
 };
 std::map<int, DeviceInfo> g_devices;
 
@@ -79,11 +79,9 @@ int device_info(int dev, DeviceInfo** out) {
     if (d.supported) {
       for (int c = 0; c < kNumConfigs; ++c) {
         if (kConfigs[c]->set_attributes() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-        for (int t = 0; t < 2; ++t) {
-          int blocks = 0;
-          if (kConfigs[c]->occupancy(t != 0, &blocks) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-          d.occupancy[c][t] = blocks;
-        }
+        int blocks = 0;
+        if (kConfigs[c]->occupancy(&blocks) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        d.occupancy[c] = blocks;
       }
     }
     d.ready = true;
@@ -143,14 +141,170 @@ int get_workspace(int dev, cudaStream_t stream, size_t flags, size_t partial_flo
 }
 
 
-__global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {
-  const long long total = (long long)M * N;
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  return SGEMM_OK;
+}
+
+// C = beta * C for `batch` matrices (beta == 0 writes zeros without reading C).
+__global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc, long long sC,
+                               int batch) {
+  const long long per = (long long)M * N;
+  const long long total = per * batch;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
-    const long long i = e / N, j = e % N;
-    float* c = C + i * ldc + j;
+    const long long bi = e / per, r = e - bi * per;
+    const long long i = r / N, j = r % N;
+    float* c = C + bi * sC + i * ldc + j;
     *c = beta == 0.f ? 0.f : beta * *c;
   }
+}
+
+// 3-D tensor map over `batch` row-major matrices of rows x cols (row pitch ld,
+// matrix pitch stride, in elements) with a box of box_cols x box_rows x 1.
+bool encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const float* base,
+               int cols, int rows, long long ld, long long stride, int batch, int box_cols,
+               int box_rows) {
+  const long long pitch2 = batch > 1 ? stride : ld * (rows > 0 ? rows : 1);
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)(((pitch2 * 4) + 15) / 16 * 16)};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Argument checks shared by every FFMA entry point; 0 when valid.
+int check_args(int opA, int opB, int M, int N, int K, float alpha, const float* A, int lda,
+               long long sA, const float* B, int ldb, long long sB, float* C, int ldc,
+               long long sC, int batch) {
+  if ((opA != SGEMM_OP_N && opA != SGEMM_OP_T) || (opB != SGEMM_OP_N && opB != SGEMM_OP_T))
+    return SGEMM_ERR_INVALID_VALUE;
+  if (M < 0 || N < 0 || K < 0 || batch < 0) return SGEMM_ERR_INVALID_DIM;
+  const int lda_min = opA == SGEMM_OP_N ? K : M;
+  const int ldb_min = opB == SGEMM_OP_N ? N : K;
+  if (lda < (lda_min > 1 ? lda_min : 1) || ldb < (ldb_min > 1 ? ldb_min : 1) ||
+      ldc < (N > 1 ? N : 1))
+    return SGEMM_ERR_INVALID_LD;
+  if (sA < 0 || sB < 0 || sC < 0) return SGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
+  const bool reads_ab = (K > 0 && alpha != 0.f);
+  if (C == nullptr || (reads_ab && (A == nullptr || B == nullptr))) return SGEMM_ERR_NULL_PTR;
+  if ((reinterpret_cast<uintptr_t>(C) & 3u) ||
+      (reads_ab && ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))))
+    return SGEMM_ERR_MISALIGNED;
+  return SGEMM_OK;
+}
+
+// The FFMA path for every operand layout and batch count (arguments checked).
+int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A, int lda,
+             long long sA, const float* B, int ldb, long long sB, float beta, float* C, int ldc,
+             long long sC, int batch, cudaStream_t stream) {
+  if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
+  const bool reads_ab = (K > 0 && alpha != 0.f);
+  int dev = 0;
+  int st = current_device(&dev);
+  if (st != SGEMM_OK) return st;
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo* di = nullptr;
+  st = device_info(dev, &di);
+  if (st != SGEMM_OK) return st;
+
+  if (!reads_ab) {
+    const long long total = (long long)M * N * batch;
+    int blocks = (int)((total + 255) / 256);
+    if (blocks > di->sms * 8) blocks = di->sms * 8;
+    scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc, sC, batch);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    snprintf(g_last_config, sizeof(g_last_config), "scale_c");
+    return SGEMM_OK;
+  }
+
+  const bool row_major = (opA == SGEMM_OP_N && opB == SGEMM_OP_N);
+  int id = g_forced.load();
+  if (id < 0 || id >= kNumConfigs || (!row_major && !kConfigs[id]->all_layouts))
+    id = choose_config(M, N, K);
+  const ConfigEntry& cfg = *kConfigs[id];
+  const TileShape& S = cfg.shape;
+
+  // operand load modes: TMA where the pointer, leading dimension and batch
+  // stride are 16-byte multiples, else 4-byte copies
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  const bool single = batch == 1;
+  CUtensorMap map_a, map_b;
+  std::memset(&map_a, 0, sizeof(map_a));
+  std::memset(&map_b, 0, sizeof(map_b));
+  int al = kARow, bl = kBRowCp;
+  if (opA == SGEMM_OP_T) {
+    al = kATCp;
+    if (enc != nullptr && ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0) &&
+        (single || (sA & 3) == 0) &&
+        encode_3d(enc, &map_a, A, M, K, lda, sA, batch, S.BM, S.BK))
+      al = kATTma;
+  }
+  if (opB == SGEMM_OP_T) {
+    bl = kBT;
+  } else if (enc != nullptr && ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) && ((ldb & 3) == 0) &&
+             (single || (sB & 3) == 0) &&
+             encode_3d(enc, &map_b, B, N, K, ldb, sB, batch, S.BN, S.BK)) {
+    bl = kBRowTma;
+  }
+
+  const int occ = di->occupancy[id];
+  if (occ < 1) return SGEMM_ERR_LAUNCH;
+  const int tiles_m = (M + S.BM - 1) / S.BM, tiles_n = (N + S.BN - 1) / S.BN;
+  const int kiters = (K + S.BK - 1) / S.BK;
+  const long long total_tiles = (long long)tiles_m * tiles_n * batch;
+  if (total_tiles > 0x7fffffffLL) return SGEMM_ERR_INVALID_DIM;
+  Schedule sched = make_schedule(tiles_m, tiles_n, kiters, di->sms * occ, kGroupM, kMinSplitUnits,
+                                 batch);
+
+  const bool split = sched.dp_tiles < sched.tiles;
+  Workspace* ws = nullptr;
+  st = get_workspace(dev, stream, (size_t)sched.grid,
+                     split ? (size_t)sched.grid * S.BM * S.BN : 0, &ws);
+  if (st != SGEMM_OK) return st;
+  if (++ws->epoch == 0) ws->epoch = 1;
+
+  KernelParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.A = A;
+  p.lda = lda;
+  p.B = B;
+  p.ldb = ldb;
+  p.C = C;
+  p.ldc = ldc;
+  p.sA = sA;
+  p.sB = sB;
+  p.sC = sC;
+  p.sched = sched;
+  p.ws = ws->partials;
+  p.flags = ws->flags;
+  p.status = ws->status;
+  p.epoch = ws->epoch;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && ((ldc & 3) == 0) &&
+            (single || (sC & 3) == 0);
+  p.timeout_ns = g_timeout_ns.load();
+
+  if (cfg.launch(al, bl, sched.grid, p, &map_a, &map_b, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  static const char* const kAName[] = {"a=rowT", "a=tma", "a=cp"};
+  static const char* const kBName[] = {"b=tma", "b=cp", "b=colT"};
+  snprintf(g_last_config, sizeof(g_last_config), "%s %s %s grid=%d dp=%d split=%d kiters=%d%s",
+           cfg.name, kAName[al], kBName[bl], sched.grid, sched.dp_tiles,
+           sched.tiles - sched.dp_tiles, sched.kiters, batch > 1 ? " batched" : "");
+  return SGEMM_OK;
 }
 
 __global__ void diag_wait_kernel(int* status, long long timeout_ns) {
@@ -166,13 +320,6 @@ __global__ void diag_wait_kernel(int* status, long long timeout_ns) {
   bounded_wait(ptx::smem_addr(&bar), 0u, &abort_w, status, kDevTimeoutFull, timeout_ns);
 }
 
-int current_device(int* dev) {
-  if (cudaGetDevice(dev) != cudaSuccess) {
-    cudaGetLastError();
-    return SGEMM_ERR_LAUNCH;
-  }
-  return SGEMM_OK;
-}
 
 }  // namespace
 
@@ -234,102 +381,32 @@ SGEMM_API const char* sgemm_status_string(int status) {
 }
 
 SGEMM_API int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
-                    int ldb, float beta, float* C, int ldc, void* stream_) {
-  // ---- host-side validation: nothing is launched on error ------------------
-  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
-  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
-    return SGEMM_ERR_INVALID_LD;
-  if (M == 0 || N == 0) return SGEMM_OK;
-  const bool reads_ab = (K > 0 && alpha != 0.f);
-  if (C == nullptr || (reads_ab && (A == nullptr || B == nullptr))) return SGEMM_ERR_NULL_PTR;
-  if ((reinterpret_cast<uintptr_t>(C) & 3u) ||
-      (reads_ab && ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))))
-    return SGEMM_ERR_MISALIGNED;
+                    int ldb, float beta, float* C, int ldc, void* stream) {
+  const int st = check_args(SGEMM_OP_N, SGEMM_OP_N, M, N, K, alpha, A, lda, 0, B, ldb, 0, C, ldc,
+                            0, 1);
+  if (st != SGEMM_OK || M == 0 || N == 0) return st;
+  return run_ffma(SGEMM_OP_N, SGEMM_OP_N, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0,
+                  1, static_cast<cudaStream_t>(stream));
+}
 
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  int dev = 0;
-  int st = current_device(&dev);
-  if (st != SGEMM_OK) return st;
+SGEMM_API int sgemm_ex(int opA, int opB, int M, int N, int K, float alpha, const float* A,
+                       int lda, const float* B, int ldb, float beta, float* C, int ldc,
+                       void* stream) {
+  const int st = check_args(opA, opB, M, N, K, alpha, A, lda, 0, B, ldb, 0, C, ldc, 0, 1);
+  if (st != SGEMM_OK || M == 0 || N == 0) return st;
+  return run_ffma(opA, opB, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1,
+                  static_cast<cudaStream_t>(stream));
+}
 
-  std::lock_guard<std::mutex> lock(g_mutex);
-  DeviceInfo* di = nullptr;
-  st = device_info(dev, &di);
-  if (st != SGEMM_OK) return st;
-
-  if (!reads_ab) {
-    // C = beta * C (beta == 0 writes zeros without reading C)
-    const long long total = (long long)M * N;
-    int blocks = (int)((total + 255) / 256);
-    if (blocks > di->sms * 8) blocks = di->sms * 8;
-    scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
-    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    snprintf(g_last_config, sizeof(g_last_config), "scale_c");
-    return SGEMM_OK;
-  }
-
-  int id = g_forced.load();
-  if (id < 0 || id >= kNumConfigs) id = choose_config(M, N, K);
-  const ConfigEntry& cfg = *kConfigs[id];
-  const TileShape& S = cfg.shape;
-
-  // B by TMA when its base is 16-byte aligned and its rows are 16-byte strided
-  bool tma = ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) && ((ldb & 3) == 0);
-  CUtensorMap map;
-  std::memset(&map, 0, sizeof(map));
-  if (tma) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    tma = false;
-    if (enc != nullptr) {
-      cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
-      cuuint64_t strides[1] = {(cuuint64_t)ldb * 4};
-      cuuint32_t box[2] = {(cuuint32_t)S.BN, (cuuint32_t)S.BK};
-      cuuint32_t estr[2] = {1, 1};
-      CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims,
-                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      tma = (r == CUDA_SUCCESS);
-    }
-  }
-
-  const int occ = di->occupancy[id][tma ? 1 : 0];
-  if (occ < 1) return SGEMM_ERR_LAUNCH;
-  const int tiles_m = (M + S.BM - 1) / S.BM, tiles_n = (N + S.BN - 1) / S.BN;
-  const int kiters = (K + S.BK - 1) / S.BK;
-  Schedule sched = make_schedule(tiles_m, tiles_n, kiters, di->sms * occ, kGroupM, kMinSplitUnits);
-
-  const bool split = sched.dp_tiles < sched.tiles;
-  Workspace* ws = nullptr;
-  st = get_workspace(dev, stream, (size_t)sched.grid,
-                     split ? (size_t)sched.grid * S.BM * S.BN : 0, &ws);
-  if (st != SGEMM_OK) return st;
-  if (++ws->epoch == 0) ws->epoch = 1;
-
-  KernelParams p;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.alpha = alpha;
-  p.beta = beta;
-  p.A = A;
-  p.lda = lda;
-  p.B = B;
-  p.ldb = ldb;
-  p.C = C;
-  p.ldc = ldc;
-  p.sched = sched;
-  p.ws = ws->partials;
-  p.flags = ws->flags;
-  p.status = ws->status;
-  p.epoch = ws->epoch;
-  p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && ((ldc & 3) == 0);
-  p.timeout_ns = g_timeout_ns.load();
-
-  if (cfg.launch(tma, sched.grid, p, &map, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-  snprintf(g_last_config, sizeof(g_last_config), "%s b=%s grid=%d dp=%d split=%d kiters=%d",
-           cfg.name, tma ? "tma" : "cp.async", sched.grid, sched.dp_tiles,
-           sched.tiles - sched.dp_tiles, sched.kiters);
-  return SGEMM_OK;
+SGEMM_API int sgemm_strided_batched(int opA, int opB, int M, int N, int K, float alpha,
+                                    const float* A, int lda, long long strideA, const float* B,
+                                    int ldb, long long strideB, float beta, float* C, int ldc,
+                                    long long strideC, int batch, void* stream) {
+  const int st = check_args(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, C, ldc,
+                            strideC, batch);
+  if (st != SGEMM_OK || M == 0 || N == 0 || batch == 0) return st;
+  return run_ffma(opA, opB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                  strideC, batch, static_cast<cudaStream_t>(stream));
 }
 
 SGEMM_API int sgemm_last_config(char* buf, int len) {

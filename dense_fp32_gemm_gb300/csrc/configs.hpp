@@ -61,15 +61,20 @@ struct KernelParams;
 SGEMM_GB300_CONFIGS(SGEMM_GB300_CFG_STRUCT)
 #undef SGEMM_GB300_CFG_STRUCT
 
-using LaunchFn = cudaError_t (*)(bool tma, int grid, const KernelParams& p, const CUtensorMap* map,
+// Launch of one operand-layout variant (al: ALoad, bl: BLoad, ffma_sgemm.cuh);
+// map_a is used when A arrives by TMA, map_b when B does. Returns
+// cudaErrorInvalidValue for a variant the configuration was not built with.
+using LaunchFn = cudaError_t (*)(int al, int bl, int grid, const KernelParams& p,
+                                 const CUtensorMap* map_a, const CUtensorMap* map_b,
                                  cudaStream_t stream);
 using AttrFn = cudaError_t (*)();
-using OccFn = cudaError_t (*)(bool tma, int* blocks_per_sm);
+using OccFn = cudaError_t (*)(int* blocks_per_sm);
 
 struct ConfigEntry {
   const char* name;
   TileShape shape;
   int smem_bytes;      // dynamic shared memory per CTA, alignment slack included
+  bool all_layouts;    // built for transposed operands too (else row-major A and B only)
   AttrFn set_attributes;
   OccFn occupancy;
   LaunchFn launch;

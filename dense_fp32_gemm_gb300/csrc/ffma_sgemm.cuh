@@ -68,6 +68,7 @@ struct KernelParams {
   long long ldb;
   float* C;
   long long ldc;
+  long long sA, sB, sC; // elements between consecutive matrices of a batch
   Schedule sched;
   float* ws;            // grid * BM * BN floats: one partial tile per CTA
   uint32_t* flags;      // grid flags: flags[b] == epoch once slot b is written
@@ -77,13 +78,24 @@ struct KernelParams {
   long long timeout_ns; // bound on every wait
 };
 
+// How each operand tile reaches shared memory (template parameters AL, BL):
+//   A: kARow   A stored M x K (op N): transposing 4-byte cp.async into As[k][m]
+//      kATTma  A stored K x M (op T): one 3-D TMA box, As[k][m] needs no transpose
+//      kATCp   A stored K x M (op T): plain 4-byte cp.async (A not TMA-aligned)
+//   B: kBRowTma B stored K x N (op N): one 3-D TMA box into Bs[k][n]
+//      kBRowCp  B stored K x N (op N): plain 4-byte cp.async
+//      kBT      B stored N x K (op T): transposing 4-byte cp.async into Bs[k][n]
+enum ALoad : int { kARow = 0, kATTma = 1, kATCp = 2 };
+enum BLoad : int { kBRowTma = 0, kBRowCp = 1, kBT = 2 };
+
 // Shared-memory layout (from a 1024-byte aligned base):
-//   Bs[STAGES][BK][BN] | As[STAGES][BK][BM + kApad] | fullA[STAGES] |
-//   fullB[STAGES] | empty[STAGES] | sync barrier | abort word
+//   Bs[STAGES][BK][BP] | As[STAGES][BK][AP] | fullA[STAGES] | fullB[STAGES] |
+//   empty[STAGES] | sync barrier | abort word
+// with row pitches AP = BM (+ kApad when transposed on store) and likewise BP.
 template <int ST>
 struct BarrierBlock {
   uint64_t fullA[ST];   // NT cp.async arrivals: this thread's copies landed
-  uint64_t fullB[ST];   // one expect_tx arrival + the TMA transaction bytes
+  uint64_t fullB[ST];   // one expect_tx arrival + the TMA transaction bytes of the stage
   uint64_t empty[ST];   // one arrival per warp: the slot may be refilled
   uint64_t sync;        // CTA-wide rendezvous with a bounded wait
   int abort;            // set by the first thread that gives up waiting
@@ -116,17 +128,18 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, vola
   }
 }
 
-// Interior A copies of one row group: for each k-group KG, one 4-byte copy
-// with both offsets compile-time (destination: KG*8 rows of As plus the
-// group's MG*A_ROWS columns; source: KG*8 floats along the row).
+// Interior transposing copies of one row group (rows of A, or of a stored
+// transposed B): for each k-group KG, one 4-byte copy with both offsets
+// compile-time (destination: KG*8 rows of the tile plus the group's
+// MG*A_ROWS columns; source: KG*8 floats along the row).
 template <int AP, int A_ROWS, int MG, int... KG>
 __device__ __forceinline__ void issue_a_group(uint32_t dst, const float* src,
                                               std::integer_sequence<int, KG...>) {
   (ptx::cp_async_4_imm<(KG * kAloadK * AP + MG * A_ROWS) * 4, KG * kAloadK * 4>(dst, src), ...);
 }
 
-// All interior A copies of one k-slice: row group MG starts MG*stride floats
-// after the first.
+// All interior transposing copies of one k-slice: row group MG starts
+// MG*stride floats after the first.
 template <int AP, int A_ROWS, int A_KG, int... MG>
 __device__ __forceinline__ void issue_a_tile(uint32_t dst, const float* src, long long stride,
                                              std::integer_sequence<int, MG...>) {
@@ -134,9 +147,10 @@ __device__ __forceinline__ void issue_a_tile(uint32_t dst, const float* src, lon
    ...);
 }
 
-template <class Cfg, bool kBTma>
+template <class Cfg, int AL, int BL>
 __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     ffma_sgemm_kernel(const __grid_constant__ KernelParams p,
+                      const __grid_constant__ CUtensorMap tmapA,
                       const __grid_constant__ CUtensorMap tmapB) {
   constexpr TileShape S = Cfg::S;
   static_assert(cfg_valid(S), "illegal tile configuration");
@@ -144,15 +158,23 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   constexpr int ORDER = S.ORDER;
   constexpr int WM = S.WM, WN = S.WN, TM = S.TM, TN = S.TN, WNITER = S.WNITER;
   constexpr int WMITER = wmiter(S), WSUBM = wsubm(S), WSUBN = wsubn(S);
-  constexpr int AP = BM + kApad;               // As row pitch (floats)
+  constexpr int AP = (AL == kARow) ? BM + kApad : BM;   // As row pitch (floats)
+  constexpr int BP = (BL == kBT) ? BN + kApad : BN;     // Bs row pitch (floats)
   constexpr int A_ST = a_stage_floats(S), B_ST = b_stage_floats(S);
+  static_assert(BK * AP <= A_ST && BK * BP <= B_ST, "stage sizes");
   constexpr int D = ST - 2;                    // k-slices loaded ahead
   constexpr int LANES_N = WSUBN / TN;          // lanes along n in a sub-tile
   constexpr int RM = WMITER * TM, RN = WNITER * TN;  // a lane's rows / cols
-  constexpr int A_ROWS = NT / kAloadK;         // rows of A per load pass
+  constexpr int A_ROWS = NT / kAloadK;         // rows per transposing-copy pass
   constexpr int A_MG = BM / A_ROWS, A_KG = BK / kAloadK;
+  constexpr int B_MG = BN / A_ROWS;            // same, for a stored transposed B
   constexpr int B_PASSES = (BK * BN) / NT;
+  constexpr int AT_PASSES = (BK * BM) / NT;
   constexpr int WARPS_N = BN / WN;
+  constexpr bool kUsesCp = (AL != kATTma) || (BL != kBRowTma);
+  constexpr bool kUsesTma = (AL == kATTma) || (BL == kBRowTma);
+  constexpr uint32_t TMA_BYTES =
+      (uint32_t)(((AL == kATTma) ? BK * BM * 4 : 0) + ((BL == kBRowTma) ? BK * BN * 4 : 0));
   constexpr uint32_t FULL = 0xffffffffu;
 
   extern __shared__ unsigned char smem_raw[];
@@ -178,7 +200,8 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     ptx::mbar_init(ptx::smem_addr(&bb->sync), NT);
     bb->abort = 0;
     ptx::mbar_fence_init();
-    if (kBTma) ptx::tma_prefetch_desc(&tmapB);
+    if (AL == kATTma) ptx::tma_prefetch_desc(&tmapA);
+    if (BL == kBRowTma) ptx::tma_prefetch_desc(&tmapB);
   }
   __syncthreads();
 
@@ -191,33 +214,39 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   // fragment read offsets inside one stage (floats)
   const int a_frag_off = warp_m * WM + lr * TM;
   const int b_frag_off = warp_n * WN + lc * TN;
-  // A loader: this thread copies k = kg*8 + a_k of rows mg*A_ROWS + a_m
+  // transposing copies: this thread copies k = kg*8 + a_k of rows mg*A_ROWS + a_m
   const int a_k = tid % kAloadK, a_m = tid / kAloadK;
-  const uint32_t a_dst0 = (uint32_t)((a_k * AP + a_m) * 4);
 
   const float* __restrict__ Ag = p.A;
   const float* __restrict__ Bg = p.B;
   const int M = p.M, N = p.N, K = p.K;
   const long long lda = p.lda, ldb = p.ldb;
   const long long a_group_stride = (long long)A_ROWS * lda;  // floats between row groups
+  const long long b_group_stride = (long long)A_ROWS * ldb;
 
   const uint32_t As_addr = ptx::smem_addr(As);
   const uint32_t Bs_addr = ptx::smem_addr(Bs);
 
   // ---- load cursor: which (tile, k-slice) the next issued step is ---------
-  int l_piece = 0, l_k = 0, l_ke = 0, l_m0 = 0, l_n0 = 0;
+  int l_piece = 0, l_k = 0, l_ke = 0, l_m0 = 0, l_n0 = 0, l_bi = 0;
   bool l_m_inside = false;            // all BM rows of the tile are < M
-  const float* l_arow = Ag;           // A + (m0 + a_m) * lda
+  bool l_n_inside = false;            // all BN columns of the tile are < N
+  const float* l_arow = Ag;           // row-major A: A + bi*sA + (m0 + a_m) * lda
+  const float* l_brow = Bg;           // stored transposed B: B + bi*sB + (n0 + a_m) * ldb
   auto set_load_piece = [&](int i) {
     const Piece lp = get_piece(sc, b, i);
     int tm, tn;
-    tile_coords(sc, lp.tile, tm, tn);
+    tile_coords_batched(sc, lp.tile, l_bi, tm, tn);
     l_k = lp.kb;
     l_ke = lp.ke;
     l_m0 = tm * BM;
     l_n0 = tn * BN;
     l_m_inside = l_m0 + BM <= M;
-    l_arow = Ag + (l_m_inside ? (long long)(l_m0 + a_m) * lda : 0);
+    l_n_inside = l_n0 + BN <= N;
+    if (AL == kARow)
+      l_arow = Ag + (long long)l_bi * p.sA + (l_m_inside ? (long long)(l_m0 + a_m) * lda : 0);
+    if (BL == kBT)
+      l_brow = Bg + (long long)l_bi * p.sB + (l_n_inside ? (long long)(l_n0 + a_m) * ldb : 0);
   };
   if (npieces > 0) set_load_piece(0);
   int issued = 0;
@@ -233,46 +262,86 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
       if (!__all_sync(FULL, ok)) return false;
     }
     const int k0 = l_k * BK;
-    // A: transposed on store, As[k][m] <- A[m0 + m][k0 + k], zero outside
-    const uint32_t a_slot = As_addr + (uint32_t)(slot * A_ST * 4) + a_dst0;
-    if (l_m_inside && k0 + BK <= K) {
-      // interior slice: no predicates, immediate offsets
-      issue_a_tile<AP, A_ROWS, A_KG>(a_slot, l_arow + k0 + a_k, a_group_stride,
-                                     std::make_integer_sequence<int, A_MG>{});
-    } else {
+    const uint32_t a_slot = As_addr + (uint32_t)(slot * A_ST * 4);
+    const uint32_t b_slot = Bs_addr + (uint32_t)(slot * B_ST * 4);
+    const uint32_t t_dst0 = (uint32_t)((a_k * AP + a_m) * 4);  // transposing-copy offsets
+    if constexpr (AL == kARow) {
+      // A transposed on store, As[k][m] <- A[m0 + m][k0 + k], zero outside
+      if (l_m_inside && k0 + BK <= K) {
+        issue_a_tile<AP, A_ROWS, A_KG>(a_slot + t_dst0, l_arow + k0 + a_k, a_group_stride,
+                                       std::make_integer_sequence<int, A_MG>{});
+      } else {
+        const float* Ab = Ag + (long long)l_bi * p.sA;
 #pragma unroll
-      for (int mg = 0; mg < A_MG; ++mg) {
-        const int row = l_m0 + mg * A_ROWS + a_m;
-        const bool row_ok = row < M;
-        const float* src_row = Ag + (row_ok ? (long long)row * lda : 0);
+        for (int mg = 0; mg < A_MG; ++mg) {
+          const int row = l_m0 + mg * A_ROWS + a_m;
+          const bool row_ok = row < M;
+          const float* src_row = Ab + (row_ok ? (long long)row * lda : 0);
 #pragma unroll
-        for (int kg = 0; kg < A_KG; ++kg) {
-          const int k = k0 + kg * kAloadK + a_k;
-          const bool ok = row_ok && (k < K);
-          ptx::cp_async_4(a_slot + (uint32_t)((kg * kAloadK * AP + mg * A_ROWS) * 4),
-                          ok ? (const void*)(src_row + k) : (const void*)Ag, ok ? 4u : 0u);
+          for (int kg = 0; kg < A_KG; ++kg) {
+            const int k = k0 + kg * kAloadK + a_k;
+            const bool ok = row_ok && (k < K);
+            ptx::cp_async_4(a_slot + t_dst0 + (uint32_t)((kg * kAloadK * AP + mg * A_ROWS) * 4),
+                            ok ? (const void*)(src_row + k) : (const void*)Ag, ok ? 4u : 0u);
+          }
         }
       }
+    } else if constexpr (AL == kATCp) {
+      // stored transposed A: As[k][m] <- A[k0 + k][m0 + m], zero outside
+      const float* Ab = Ag + (long long)l_bi * p.sA;
+#pragma unroll
+      for (int ps = 0; ps < AT_PASSES; ++ps) {
+        const int e = ps * NT + tid;
+        const int kk = e / BM, mm = e % BM;
+        const int k = k0 + kk, m = l_m0 + mm;
+        const bool ok = (k < K) && (m < M);
+        ptx::cp_async_4(a_slot + (uint32_t)((kk * AP + mm) * 4),
+                        ok ? (const void*)(Ab + (long long)k * lda + m) : (const void*)Ag,
+                        ok ? 4u : 0u);
+      }
     }
-    if (!kBTma) {
+    if constexpr (BL == kBRowCp) {
       // B without TMA: Bs[k][n] <- B[k0 + k][n0 + n], zero outside
-      const uint32_t b_slot = Bs_addr + (uint32_t)(slot * B_ST * 4);
+      const float* Bb = Bg + (long long)l_bi * p.sB;
 #pragma unroll
       for (int ps = 0; ps < B_PASSES; ++ps) {
         const int e = ps * NT + tid;
         const int kk = e / BN, nn = e % BN;
         const int k = k0 + kk, n = l_n0 + nn;
         const bool ok = (k < K) && (n < N);
-        ptx::cp_async_4(b_slot + (uint32_t)(e * 4),
-                        ok ? (const void*)(Bg + (long long)k * ldb + n) : (const void*)Bg,
+        ptx::cp_async_4(b_slot + (uint32_t)((kk * BP + nn) * 4),
+                        ok ? (const void*)(Bb + (long long)k * ldb + n) : (const void*)Bg,
                         ok ? 4u : 0u);
       }
+    } else if constexpr (BL == kBT) {
+      // stored transposed B: Bs[k][n] <- B[n0 + n][k0 + k], transposed on store
+      const uint32_t bt_dst0 = (uint32_t)((a_k * BP + a_m) * 4);
+      if (l_n_inside && k0 + BK <= K) {
+        issue_a_tile<BP, A_ROWS, A_KG>(b_slot + bt_dst0, l_brow + k0 + a_k, b_group_stride,
+                                       std::make_integer_sequence<int, B_MG>{});
+      } else {
+        const float* Bb = Bg + (long long)l_bi * p.sB;
+#pragma unroll
+        for (int ng = 0; ng < B_MG; ++ng) {
+          const int row = l_n0 + ng * A_ROWS + a_m;
+          const bool row_ok = row < N;
+          const float* src_row = Bb + (row_ok ? (long long)row * ldb : 0);
+#pragma unroll
+          for (int kg = 0; kg < A_KG; ++kg) {
+            const int k = k0 + kg * kAloadK + a_k;
+            const bool ok = row_ok && (k < K);
+            ptx::cp_async_4(b_slot + bt_dst0 + (uint32_t)((kg * kAloadK * BP + ng * A_ROWS) * 4),
+                            ok ? (const void*)(src_row + k) : (const void*)Bg, ok ? 4u : 0u);
+          }
+        }
+      }
     }
-    ptx::cp_async_arrive_noinc(ptx::smem_addr(&bb->fullA[slot]));
-    if (kBTma && tid == 0) {
+    if (kUsesCp) ptx::cp_async_arrive_noinc(ptx::smem_addr(&bb->fullA[slot]));
+    if (kUsesTma && tid == 0) {
       const uint32_t fb = ptx::smem_addr(&bb->fullB[slot]);
-      ptx::mbar_arrive_expect_tx(fb, (uint32_t)(BK * BN * 4));
-      ptx::tma_load_2d(Bs_addr + (uint32_t)(slot * B_ST * 4), &tmapB, l_n0, k0, fb);
+      ptx::mbar_arrive_expect_tx(fb, TMA_BYTES);
+      if (AL == kATTma) ptx::tma_load_3d(a_slot, &tmapA, l_m0, k0, l_bi, fb);
+      if (BL == kBRowTma) ptx::tma_load_3d(b_slot, &tmapB, l_n0, k0, l_bi, fb);
     }
     ++issued;
     if (++l_k == l_ke) {
@@ -281,25 +350,26 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     return true;
   };
 
-  // Non-blocking test: have both operand tiles of `step` landed? (Both
-  // barriers are polled at once so their latencies overlap.)
+  // Non-blocking test: have the operand tiles of `step` landed? (The copy
+  // and TMA barriers are polled at once so their latencies overlap.)
   auto test_full = [&](int step) -> bool {
     const int slot = step % ST;
     const uint32_t par = (uint32_t)((step / ST) & 1);
-    const bool a = ptx::mbar_try_wait(ptx::smem_addr(&bb->fullA[slot]), par);
-    const bool b2 = kBTma ? ptx::mbar_try_wait(ptx::smem_addr(&bb->fullB[slot]), par) : true;
+    const bool a = kUsesCp ? ptx::mbar_try_wait(ptx::smem_addr(&bb->fullA[slot]), par) : true;
+    const bool b2 = kUsesTma ? ptx::mbar_try_wait(ptx::smem_addr(&bb->fullB[slot]), par) : true;
     return a && b2;
   };
-  // Bounded wait until both operand tiles of `step` have landed; `ready` is
+  // Bounded wait until the operand tiles of `step` have landed; `ready` is
   // the result of an earlier test_full(step), if one was made.
   auto wait_full = [&](int step, bool ready) -> bool {
     bool ok = true;
     if (!ready) {
       const int slot = step % ST;
       const uint32_t par = (uint32_t)((step / ST) & 1);
-      ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
-                        kDevTimeoutFull, p.timeout_ns);
-      if (kBTma && ok)
+      if (kUsesCp)
+        ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
+                          kDevTimeoutFull, p.timeout_ns);
+      if (kUsesTma && ok)
         ok = bounded_wait(ptx::smem_addr(&bb->fullB[slot]), par, abort_w, p.status,
                           kDevTimeoutFull, p.timeout_ns);
     }
@@ -317,7 +387,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     for (int j = 0; j < RN; ++j) acc2[i][j] = make_float2(0.f, 0.f);
 #define SG_ACC(i, j) (((i) & 1) ? acc2[(i) >> 1][j].y : acc2[(i) >> 1][j].x)
 
-  // Two fragment buffers: while the FFMAs of k-step k read one, the 128-bit
+  // Two fragment buffers: while the FMAs of k-step k read one, the 128-bit
   // loads of k-step k+1 fill the other.
   float af[2][RM], bfr[2][RN];
   auto load_frags = [&](int buf, const float* a_row, const float* b_row) {
@@ -387,7 +457,6 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     const float* b_s = Bs + slot * B_ST + b_frag_off;
     bool next_ok = true;
 
-
     // ---- BK k-steps of outer-product FMA on this slot, KU per chunk ----------
     // One k-step: update the accumulators from fragment buffer `cur`.
     auto kstep = [&](int cur) {
@@ -423,7 +492,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 #pragma unroll
       for (int kk = 0; kk < KU; ++kk) {
         const int cur = kk & 1;
-        load_frags(cur ^ 1, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BN);
+        load_frags(cur ^ 1, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BP);
         kstep(cur);
       }
     }
@@ -437,7 +506,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
       for (int kk = 0; kk < KU; ++kk) {
         const int cur = kk & 1;
         if (kk + 1 < KU) {
-          load_frags(cur ^ 1, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BN);
+          load_frags(cur ^ 1, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BP);
           if (kk == KU / 2 - 1 && has_next) ready = test_full(step + 1);
         } else if (has_next) {
           next_ok = wait_full(step + 1, ready);
@@ -519,8 +588,9 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
       // one row group (TM rows x RN columns) at a time: all of the group's
       // 128-bit reads of C are issued before any of its writes, so their
       // latencies overlap instead of adding up.
-      int tm, tn;
-      tile_coords(sc, cpc.tile, tm, tn);
+      int bi, tm, tn;
+      tile_coords_batched(sc, cpc.tile, bi, tm, tn);
+      float* Cb = p.C + (long long)bi * p.sC;
       const int row0 = tm * BM + a_frag_off;
       const int col0 = tn * BN + b_frag_off;
       const float alpha = p.alpha, beta = p.beta;
@@ -534,7 +604,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 #pragma unroll
           for (int g = 0; g < QN; ++g) {
             const int col = col0 + (g / (TN / 4)) * WSUBN + (g % (TN / 4)) * 4;
-            const float* cp = p.C + (long long)row * p.ldc + col;
+            const float* cp = Cb + (long long)row * p.ldc + col;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (beta != 0.f && row < M) {
               if (p.c_vec && col + 3 < N) {
@@ -553,7 +623,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
         for (int i = 0; i < TM; ++i) {
           const int row = row0 + wm * WSUBM + i;
           if (row >= M) continue;
-          float* crow = p.C + (long long)row * p.ldc;
+          float* crow = Cb + (long long)row * p.ldc;
           const int ai = wm * TM + i;
 #pragma unroll
           for (int g = 0; g < QN; ++g) {
@@ -593,10 +663,10 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 
   if (aborted) {
     // Drain this thread's copies; the TMA issuer also waits (bounded) for
-    // the B tiles it issued and nobody consumed, so nothing lands in shared
+    // the tiles it issued and nobody consumed, so nothing lands in shared
     // memory after the CTA is gone.
     ptx::cp_async_wait_all();
-    if (kBTma && tid == 0) {
+    if (kUsesTma && tid == 0) {
       const uint64_t t0 = ptx::global_ns();
       for (int s = issued - 1; s >= 0 && s >= issued - ST; --s) {
         const uint32_t fb = ptx::smem_addr(&bb->fullB[s % ST]);

@@ -70,7 +70,7 @@ constexpr int kNoAllocNumConfigs = sizeof(kNoAllocConfigs) / sizeof(kNoAllocConf
 struct NoAllocDevice {
   bool ready;
   int sms;
-  int occupancy[kNoAllocNumConfigs][2];
+  int occupancy[kNoAllocNumConfigs];
   unsigned char* base;  // device address of g_noalloc_scratch on this device
   uint32_t epoch;
 };
@@ -109,14 +109,12 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
       }
-      for (int t = 0; t < 2; ++t) {
-        int blocks = 0;
-        if (kNoAllocConfigs[c]->occupancy(t != 0, &blocks) != cudaSuccess) {
-          cudaGetLastError();
-          return SGEMM_ERR_LAUNCH;
-        }
-        d.occupancy[c][t] = blocks;
+      int blocks = 0;
+      if (kNoAllocConfigs[c]->occupancy(&blocks) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
       }
+      d.occupancy[c] = blocks;
     }
     d.base = static_cast<unsigned char*>(ptr);
     d.epoch = 0;
@@ -192,24 +190,27 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   const TileShape& S = cfg.shape;
 
   bool tma = ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) && ((ldb & 3) == 0);
-  CUtensorMap map;
-  std::memset(&map, 0, sizeof(map));
+  CUtensorMap map_a, map_b;
+  std::memset(&map_a, 0, sizeof(map_a));
+  std::memset(&map_b, 0, sizeof(map_b));
   if (tma) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = noalloc_encoder();
     tma = false;
     if (enc != nullptr) {
-      cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
-      cuuint64_t strides[1] = {(cuuint64_t)ldb * 4};
-      cuuint32_t box[2] = {(cuuint32_t)S.BN, (cuuint32_t)S.BK};
-      cuuint32_t estr[2] = {1, 1};
-      tma = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(B), dims, strides,
+      // one matrix: a 3-D map with a batch extent of 1
+      cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, 1};
+      cuuint64_t strides[2] = {(cuuint64_t)ldb * 4,
+                               (cuuint64_t)(((long long)ldb * (K > 0 ? K : 1) * 4 + 15) / 16 * 16)};
+      cuuint32_t box[3] = {(cuuint32_t)S.BN, (cuuint32_t)S.BK, 1};
+      cuuint32_t estr[3] = {1, 1, 1};
+      tma = enc(&map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(B), dims, strides,
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
   }
 
-  const int occ = d->occupancy[id][tma ? 1 : 0];
+  const int occ = d->occupancy[id];
   if (occ < 1) return SGEMM_ERR_LAUNCH;
   const Schedule sched =
       make_schedule((M + S.BM - 1) / S.BM, (N + S.BN - 1) / S.BN, (K + S.BK - 1) / S.BK,
@@ -244,6 +245,9 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   p.ldb = ldb;
   p.C = C;
   p.ldc = ldc;
+  p.sA = 0;
+  p.sB = 0;
+  p.sC = 0;
   p.sched = sched;
   p.ws = partials;
   p.flags = flags;
@@ -251,7 +255,8 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   p.epoch = d->epoch;
   p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && ((ldc & 3) == 0);
   p.timeout_ns = 4000000000LL;
-  if (cfg.launch(tma, sched.grid, p, &map, stream) != cudaSuccess) {
+  if (cfg.launch(kARow, tma ? kBRowTma : kBRowCp, sched.grid, p, &map_a, &map_b, stream) !=
+      cudaSuccess) {
     cudaGetLastError();
     return SGEMM_ERR_LAUNCH;
   }

@@ -38,8 +38,8 @@
 namespace sgemm_gb300 {
 
 struct Schedule {
-  int tiles_m, tiles_n;   // tile grid over C
-  int tiles;              // tiles_m * tiles_n
+  int tiles_m, tiles_n;   // tile grid over one C
+  int tiles;              // batch * tiles_m * tiles_n (the batch index is outermost)
   int kiters;             // k-slices per tile: ceil(K / BK)
   int grid;               // persistent CTAs
   int group_m;            // raster group height in tiles
@@ -65,6 +65,13 @@ SG_HD void tile_coords(const Schedule& s, int t, int& tm, int& tn) {
   const int r = t - group * per_group;
   tm = first + r % rows;
   tn = r / rows;
+}
+
+// Tile index -> (matrix of the batch, tile row, tile column).
+SG_HD void tile_coords_batched(const Schedule& s, int t, int& bi, int& tm, int& tn) {
+  const int per_matrix = s.tiles_m * s.tiles_n;
+  bi = t / per_matrix;
+  tile_coords(s, t - bi * per_matrix, tm, tn);
 }
 
 SG_HD int num_dp_pieces(const Schedule& s, int b) {
@@ -135,15 +142,15 @@ SG_HD bool is_partial_piece(const Schedule& s, const Piece& p) {
   return p.tile >= s.dp_tiles && p.kb != 0;
 }
 
-// Host-side choice of the decomposition for a problem of tiles_m x tiles_n
-// tiles with kiters k-slices each on `capacity` resident CTA slots.
+// Host-side choice of the decomposition for a problem of batch x tiles_m x
+// tiles_n tiles with kiters k-slices each on `capacity` resident CTA slots.
 // min_units: the fewest k-slices worth giving one CTA in a split.
 inline Schedule make_schedule(int tiles_m, int tiles_n, int kiters, int capacity, int group_m,
-                              int min_units) {
+                              int min_units, int batch = 1) {
   Schedule s{};
   s.tiles_m = tiles_m;
   s.tiles_n = tiles_n;
-  s.tiles = tiles_m * tiles_n;
+  s.tiles = tiles_m * tiles_n * batch;
   s.kiters = kiters;
   s.group_m = group_m < 1 ? 1 : (group_m > tiles_m ? tiles_m : group_m);
   if (s.group_m < 1) s.group_m = 1;

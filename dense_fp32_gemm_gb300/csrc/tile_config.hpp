@@ -52,8 +52,13 @@ constexpr int acc_per_thread(const TileShape& s) { return wmiter(s) * s.TM * s.W
 constexpr int est_registers(const TileShape& s) {
   return acc_per_thread(s) + 2 * (wmiter(s) * s.TM + s.WNITER * s.TN) + 24;
 }
-constexpr int a_stage_floats(const TileShape& s) { return s.BK * (s.BM + kApad); }
-constexpr int b_stage_floats(const TileShape& s) { return s.BK * s.BN; }
+// Floats reserved per stage for each operand tile: BK rows of the tile's width
+// plus the padding a transposing copy needs, rounded up to 1024 bytes so that
+// every stage of either operand can be a TMA destination. One size serves all
+// operand layouts (the padding is unused when a tile arrives by TMA).
+constexpr int round_1k_floats(int floats) { return (floats + 255) / 256 * 256; }
+constexpr int a_stage_floats(const TileShape& s) { return round_1k_floats(s.BK * (s.BM + kApad)); }
+constexpr int b_stage_floats(const TileShape& s) { return round_1k_floats(s.BK * (s.BN + kApad)); }
 // Dynamic shared memory of one CTA: 1024 bytes of alignment slack, the stage
 // buffers, then 3 mbarriers per stage (A landed, B landed, slot free), one
 // rendezvous barrier and an abort word.
@@ -88,9 +93,14 @@ constexpr int cfg_check(const TileShape& s) {
   if (s.BK % kAloadK != 0) return 11;
   if (s.BM % (s.NT / kAloadK) != 0 || s.BM % 32 != 0) return 12;
   // 7. B tile: one TMA box of BK rows x BN columns; the cp.async fallback
-  //    covers the tile in whole passes of NT consecutive elements
+  //    covers the tile in whole passes of NT consecutive elements; a stored
+  //    transposed B goes through the same transposing copy as A (rule 6 with
+  //    BN for BM); a stored transposed A arrives as one TMA box of BK x BM or
+  //    in whole passes of NT elements
   if (s.BN > kTmaMaxBox || s.BK > kTmaMaxBox || (s.BN * 4) % 16 != 0) return 13;
   if ((s.BK * s.BN) % s.NT != 0) return 14;
+  if (s.BN % (s.NT / kAloadK) != 0 || s.BN % 32 != 0) return 23;
+  if (s.BM > kTmaMaxBox || (s.BK * s.BM) % s.NT != 0) return 24;
   // 8. every C element owned by exactly one lane
   if (static_cast<long>(s.NT) * acc_per_thread(s) != static_cast<long>(s.BM) * s.BN) return 15;
   // 9. pipeline: at least one stage of slack between producer and consumer

@@ -53,6 +53,12 @@ typedef enum {
                                        than its fixed buffer holds             */
 } sgemm_status;
 
+/* Operand forms of sgemm_ex / sgemm_strided_batched (row-major storage). */
+typedef enum {
+  SGEMM_OP_N = 0, /* the operand as stored                               */
+  SGEMM_OP_T = 1  /* its transpose: A stored K x M, or B stored N x K     */
+} sgemm_op;
+
 /*
  * C = alpha * A * B + beta * C (FP32, FFMA path).
  *
@@ -79,6 +85,33 @@ int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float
  */
 int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
                  int ldb, float beta, float* C, int ldc, void* stream);
+
+/*
+ * C = alpha * op(A) * op(B) + beta * C, row-major, FFMA path. op(A) is M x K:
+ * A itself (SGEMM_OP_N, stored M x K, lda >= max(1, K)) or the transpose of an
+ * A stored K x M (SGEMM_OP_T, lda >= max(1, M)); op(B) is K x N: B (stored
+ * K x N, ldb >= max(1, N)) or the transpose of a B stored N x K (ldb >=
+ * max(1, K)). A stored transposed A arrives by TMA (no transposing copy); a
+ * stored transposed B goes through the transposing copy the kernel uses for
+ * row-major A. Column-major callers: a column-major M x N result is the
+ * row-major N x M result of op(B)^T op(A)^T, i.e. call with the operands and
+ * M, N swapped. Otherwise as sgemm(); SGEMM_ERR_INVALID_VALUE for another op.
+ */
+int sgemm_ex(int opA, int opB, int M, int N, int K, float alpha, const float* A, int lda,
+             const float* B, int ldb, float beta, float* C, int ldc, void* stream);
+
+/*
+ * `batch` independent products C_i = alpha * op(A_i) * op(B_i) + beta * C_i
+ * with A_i = A + i * strideA, B_i = B + i * strideB, C_i = C + i * strideC
+ * (strides in elements, >= 0; a zero stride reuses one matrix for every i,
+ * which is only valid for A and B). One launch covers every product: the
+ * batch index is the outermost tile coordinate of the persistent schedule.
+ * C_i must not overlap each other or any A_j, B_j. batch == 0 does nothing.
+ */
+int sgemm_strided_batched(int opA, int opB, int M, int N, int K, float alpha, const float* A,
+                          int lda, long long strideA, const float* B, int ldb, long long strideB,
+                          float beta, float* C, int ldc, long long strideC, int batch,
+                          void* stream);
 
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* sgemm_status_string(int status);

@@ -44,6 +44,14 @@ def test_validation_happens_before_any_device_call():
     assert binding.sgemm(4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 0, 4, None) == binding.SGEMM_ERR_NULL_PTR
     assert binding.sgemm(4, 4, 4, 1.0, 18, 4, 16, 4, 0.0, 16, 4, None) == binding.SGEMM_ERR_MISALIGNED
     assert binding.sgemm(0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4, None) == binding.SGEMM_OK
+    T = binding.SGEMM_OP_T
+    assert binding.sgemm_ex(T, 0, 8, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_LD
+    assert binding.sgemm_ex(0, T, 4, 8, 6, 1.0, 16, 6, 16, 5, 0.0, 16, 8, None) == binding.SGEMM_ERR_INVALID_LD
+    assert binding.sgemm_ex(3, 0, 4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_VALUE
+    assert binding.sgemm_strided_batched(0, 0, 4, 4, 4, 1.0, 16, 4, 16, 16, 4, 16, 0.0, 16, 4, 16, -1,
+                                         None) == binding.SGEMM_ERR_INVALID_DIM
+    assert binding.sgemm_strided_batched(0, 0, 4, 4, 4, 1.0, 16, 4, 16, 16, 4, 16, 0.0, 16, 4, 16, 0,
+                                         None) == binding.SGEMM_OK
 
 
 def test_config_registry():
