@@ -1,5 +1,5 @@
 """ctypes binding of libsgemm_gb300.so: the C ABI of include/sgemm_gb300.h
-under the same names, plus two torch conveniences that only marshal arguments
+under the same names, plus a torch convenience that only marshals arguments
 (device tensors -> pointers and leading dimensions, the current stream).
 
 There is no fallback: if the CUDA library is not built, every call raises.
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_choose_config": (I, [I, I, I, IP]),
                 "sgemm_3xtf32": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_ex": (I, [I, I, I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_host": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
                                               I, P]),
             }
@@ -98,6 +99,12 @@ def sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
     """Raw call: A, B, C are device addresses (ints), stream a cudaStream_t
     handle (int) or None. Returns the status code."""
     return lib().sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """C = alpha*A*B + beta*C on HOST matrices (addresses as ints), copies
+    overlapped with the GEMM; C is final once `stream` is synchronised."""
+    return lib().sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
 
 
 def sgemm_ex(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
@@ -247,32 +254,3 @@ def gemm(A, B, C, alpha=1.0, beta=0.0, stream=None):
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm")
     return C
-
-
-class HostGemm:
-    """End-to-end SGEMM on host (pinned) matrices: copies A, B and C to
-    device buffers it keeps, calls sgemm on `stream`, copies C back. The
-    device buffers are allocated once per shape by torch."""
-
-    def __init__(self, M, N, K, device="cuda"):
-        import torch
-        self.M, self.N, self.K = M, N, K
-        self.dA = torch.empty((M, K), dtype=torch.float32, device=device)
-        self.dB = torch.empty((K, N), dtype=torch.float32, device=device)
-        self.dC = torch.empty((M, N), dtype=torch.float32, device=device)
-
-    def h2d_bytes(self, beta):
-        return 4 * (self.M * self.K + self.K * self.N + (self.M * self.N if beta != 0 else 0))
-
-    def d2h_bytes(self):
-        return 4 * self.M * self.N
-
-    def __call__(self, hA, hB, hC, alpha, beta, stream=None):
-        """hA, hB, hC: pinned host tensors; hC receives the result."""
-        self.dA.copy_(hA, non_blocking=True)
-        self.dB.copy_(hB, non_blocking=True)
-        if beta != 0:
-            self.dC.copy_(hC, non_blocking=True)
-        gemm(self.dA, self.dB, self.dC, alpha, beta, stream)
-        hC.copy_(self.dC, non_blocking=True)
-        return hC

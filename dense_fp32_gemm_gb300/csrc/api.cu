@@ -358,6 +358,13 @@ void note_last_config(const char* text) { snprintf(g_last_config, sizeof(g_last_
 
 long long library_wait_timeout_ns() { return g_timeout_ns.load(); }
 
+// The FFMA path on device matrices (row-major, arguments already checked).
+int library_ffma(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                 int ldb, float beta, float* C, int ldc, cudaStream_t stream) {
+  return run_ffma(SGEMM_OP_N, SGEMM_OP_N, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1,
+                  stream);
+}
+
 }  // namespace sgemm_gb300
 
 using namespace sgemm_gb300;
@@ -439,7 +446,12 @@ SGEMM_API int sgemm_poll_device_status(void* stream_, int* detail) {
   return SGEMM_OK;
 }
 
+namespace sgemm_gb300 {
+void host_api_release();
+}
+
 SGEMM_API void sgemm_shutdown(void) {
+  sgemm_gb300::host_api_release();
   std::lock_guard<std::mutex> lock(g_mutex);
   int cur = 0;
   const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;

@@ -473,6 +473,17 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 #pragma unroll
           for (int j = 0; j < RN; ++j) acc2[ip][j] = __ffma2_rn(a2, bd[j], acc2[ip][j]);
         }
+      } else if constexpr (ORDER == 3) {
+        // paired FMA, column by column: one duplicated B pair feeds RM/2
+        // consecutive instructions
+#pragma unroll
+        for (int j = 0; j < RN; ++j) {
+          const float2 bd = make_float2(bfr[cur][j], bfr[cur][j]);
+#pragma unroll
+          for (int ip = 0; ip < RM / 2; ++ip)
+            acc2[ip][j] = __ffma2_rn(make_float2(af[cur][2 * ip], af[cur][2 * ip + 1]), bd,
+                                     acc2[ip][j]);
+        }
       } else {
         // scalar outer product; ORDER 1 walks odd rows backwards so that
         // consecutive FFMAs at a row change still share their B operand

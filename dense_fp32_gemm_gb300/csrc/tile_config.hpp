@@ -41,7 +41,8 @@ struct TileShape {
   int MINB;              // CTAs per SM promised to the register allocator
   int KU;                // k-steps per unrolled chunk of the inner loop
   int ORDER;             // k-step update: 0 FFMA row by row, 1 FFMA zig-zag,
-                         // 2 paired FMA (two rows of a column per instruction)
+                         // 2 paired FMA (two rows of a column per instruction),
+                         // 3 paired FMA column by column
 };
 
 // Derived quantities; valid only for shapes that pass cfg_valid().
@@ -73,7 +74,7 @@ constexpr int cfg_check(const TileShape& s) {
   // 1. positive extents
   if (s.BM <= 0 || s.BN <= 0 || s.BK <= 0 || s.WM <= 0 || s.WN <= 0 || s.WNITER <= 0 ||
       s.TM <= 0 || s.TN <= 0 || s.NT <= 0 || s.STAGES <= 0 || s.MINB <= 0 || s.KU <= 0 ||
-      s.ORDER < 0 || s.ORDER > 2)
+      s.ORDER < 0 || s.ORDER > 3)
     return 1;
   // 2. whole warps, and warp tiles that tile the CTA tile one warp each
   if (s.NT % kWarp != 0) return 2;

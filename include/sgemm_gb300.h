@@ -113,6 +113,22 @@ int sgemm_strided_batched(int opA, int opB, int M, int N, int K, float alpha, co
                           float beta, float* C, int ldc, long long strideC, int batch,
                           void* stream);
 
+/*
+ * The same C = alpha * A * B + beta * C with A, B and C in HOST memory (pinned
+ * memory gives full copy bandwidth; pageable memory works but the copies may
+ * block the calling thread). K is cut into chunks whose host -> device copies
+ * overlap the multiplication of the previous chunk on the GPU; the incoming C
+ * (read only when beta != 0) is added by one elementwise pass at the end;
+ * the result is copied back. All work is queued behind earlier work on
+ * `stream`, and `stream` waits for the final copy: once the caller has
+ * synchronised `stream`, C holds the result. The host buffers must stay
+ * valid until then. Device buffers, two copy streams and their events are
+ * owned by the library per (device, stream) and reused by later calls (freed
+ * by sgemm_shutdown). Same argument checks and status codes as sgemm().
+ */
+int sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+               float beta, float* C, int ldc, void* stream);
+
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* sgemm_status_string(int status);
 
@@ -132,8 +148,8 @@ int sgemm_last_config(char* buf, int len);
  */
 int sgemm_poll_device_status(void* stream, int* detail);
 
-/* Frees every workspace the library allocated (after synchronising the
- * device). Later calls allocate again. */
+/* Frees every workspace, device buffer, stream and event the library
+ * allocated (after synchronising the device). Later calls allocate again. */
 void sgemm_shutdown(void);
 
 /*
@@ -142,7 +158,7 @@ void sgemm_shutdown(void);
  * parameters of configuration `id` as
  * {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB, KU, ORDER} in
  * params[13] (KU: k-steps per unrolled chunk; ORDER: 0 row-by-row FFMA, 1 zig-zag
- * FFMA, 2 paired FMA).
+ * FFMA, 2 paired FMA, 3 paired FMA column by column).
  */
 int sgemm_config_count(void);
 int sgemm_config_info(int id, char* name, int len, int* params);

@@ -70,5 +70,5 @@ def test_illegal_tuples_name_their_rule(params, rule):
 def test_no_division_by_zero_on_degenerate_tuples():
     for bad in ([0] * 13, [1] * 13, [128, 64, 16, 0, 0, 0, 0, 0, 128, 3, 1, 4, 0],
                 [-128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1, 4, 0],
-                [128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1, 4, 3]):
+                [128, 64, 16, 64, 32, 2, 4, 4, 128, 3, 1, 4, 4]):
         assert binding.sgemm_cfg_check(bad)[0] != 0
