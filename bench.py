@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import datetime as _dt
+import functools
 import glob
 import hashlib
 import json
@@ -439,10 +440,123 @@ REPORT_WORKLOADS = ["square128", "square128_int", "square4096", "edges8191x1000x
                     "kdominant1024x1024x16384", "skinny16384x64x4096"] + \
     [f"sweep{n}" for n in (256, 512, 1024, 2048, 4096, 8192, 16384)]
 
+# The pages' own measurements of their kernels at M = N = K = 4096 on an
+# RTX 5080 (another GPU: context for the ladder lines, not a target):
+# "Shared Memory Tiling", section "The Arithmetic"; "Vectorized Memory Access:
+# 128-bit Loads and Stores", section "Mechanics"; "Warp Tiling: A Third Level
+# of Tiling", section "Mechanics".
+PAGES_LADDER_GFLOPS = {3: 4131.3, 7: 25130.5, 8: 29376.6}
+
+
+def _mean_ms(call, reps):
+    """Mean device time of `reps` back-to-back calls (one event pair)."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def _per_call_ms(call, reps, flush=None):
+    """Sorted device times of `reps` calls, one event pair around each; with
+    `flush`, a write larger than L2 runs before every call (outside the
+    events)."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        if flush is not None:
+            flush()
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    return sorted(a.elapsed_time(b) for a, b in ev)
+
+
+def _reps_for(call, budget_ms=200.0):
+    import torch
+    call()
+    torch.cuda.synchronize()
+    one = _mean_ms(call, 1)
+    return max(10, int(budget_ms / max(one, 1e-3)))
+
+
+def _timing_fields(call, reps, flush):
+    """mean (back to back), the per-call distribution, and the per-call
+    median with L2 flushed before each call."""
+    ms = _mean_ms(call, reps)
+    per = _per_call_ms(call, min(reps, 500))
+    fl = _per_call_ms(call, min(reps, 100), flush=flush)
+    return ms, {"ms_min": round(per[0], 5), "ms_median": round(per[len(per) // 2], 5),
+                "ms_max": round(per[-1], 5),
+                "spread_pct": round(100 * (per[-1] - per[0]) / per[len(per) // 2], 1),
+                "ms_median_l2_flushed": round(fl[len(fl) // 2], 5)}
+
+
+def _l2_flusher():
+    import torch
+    buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    return lambda: buf.fill_(1.0)
+
 
 def run_report(args):
-    """One JSON line per workload: device-timed GFLOP/s of the automatic
-    configuration and its fraction of the FFMA peak (not the default line)."""
+    """One JSON line per workload and path: device-timed GFLOP/s of the
+    automatic configuration, its fraction of the FFMA peak (the opt-in 3xTF32
+    path: of its tensor roof), the per-call time distribution and the time
+    with L2 flushed before each call. Not the default line."""
+    import torch
+
+    from dense_fp32_gemm_gb300 import binding
+    from dense_fp32_gemm_gb300.workloads import WORKLOADS, make_inputs
+    props = torch.cuda.get_device_properties(0)
+    peaks = measured_peaks()
+    max_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
+    peak_tf = ffma_peak_tflops(props.multi_processor_count, max_mhz)
+    p3 = tf32x3_peak_tflops(peaks)
+    s = torch.cuda.current_stream().cuda_stream
+    flush = _l2_flusher()
+    for name in REPORT_WORKLOADS:
+        w = WORKLOADS[name]
+        A, B, C = make_inputs(w)
+        dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+        mb = min_bytes(w.M, w.N, w.K, w.beta)
+        for path, fn in (("ffma", binding.sgemm), ("3xtf32", binding.sgemm_3xtf32)):
+            def call(fn=fn):
+                st = fn(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(), w.LDB, w.beta,
+                        dC.data_ptr(), w.LDC, s)
+                if st != 0:
+                    raise RuntimeError(binding.sgemm_status_string(st))
+            for _ in range(max(3, args.warmup)):
+                call()
+            torch.cuda.synchronize()
+            reps = _reps_for(call)
+            ms, dist = _timing_fields(call, reps, flush)
+            st, _ = binding.sgemm_poll_device_status(s)
+            tf = gemm_flops(w.M, w.N, w.K) / ms / 1e9
+            line = {"workload": name, "path": path, "M": w.M, "N": w.N, "K": w.K,
+                    "alpha": w.alpha, "beta": w.beta, "ms": round(ms, 5),
+                    "gflops": round(tf * 1e3, 1)}
+            if path == "ffma":
+                line["pct_of_ffma_peak"] = round(100 * tf / peak_tf, 2)
+            else:
+                line["pct_of_3xtf32_tensor_roof"] = round(100 * tf / p3, 2) if p3 else None
+            line.update({"min_bytes": mb, "achieved_min_gbs": round(mb / ms / 1e6, 1),
+                         "achieved_min_gbs_l2_flushed":
+                             round(mb / dist["ms_median_l2_flushed"] / 1e6, 1)})
+            line.update(dist)
+            line.update({"reps": reps, "status": st, "config": binding.sgemm_last_config()})
+            print(json.dumps(line), flush=True)
+        del dA, dB, dC
+        torch.cuda.empty_cache()
+
+
+def run_ladder(args):
+    """The pages' kernels 3, 7 and 8 next to the library's own kernel on one
+    workload (default: the 4096 cube), one JSON line each."""
     import torch
 
     from dense_fp32_gemm_gb300 import binding
@@ -452,67 +566,45 @@ def run_report(args):
     max_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
     peak_tf = ffma_peak_tflops(props.multi_processor_count, max_mhz)
     s = torch.cuda.current_stream().cuda_stream
-    for name in REPORT_WORKLOADS:
-        w = WORKLOADS[name]
-        A, B, C = make_inputs(w)
-        dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
-
-        def call():
-            st = binding.sgemm(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(),
-                               w.LDB, w.beta, dC.data_ptr(), w.LDC, s)
+    flush = _l2_flusher()
+    w = WORKLOADS[args.workload]
+    A, B, C = make_inputs(w)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    runs = [(f"ladder_kernel{k}", functools.partial(binding.sgemm_ladder, k), k)
+            for k in binding.LADDER_KERNELS] + [("sgemm", binding.sgemm, None)]
+    base_ms = None
+    lines = []
+    for path, fn, k in runs:
+        def call(fn=fn):
+            st = fn(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(), w.LDB, w.beta,
+                    dC.data_ptr(), w.LDC, s)
             if st != 0:
                 raise RuntimeError(binding.sgemm_status_string(st))
         for _ in range(max(3, args.warmup)):
             call()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        call()
-        e1.record()
-        torch.cuda.synchronize()
-        reps = max(10, int(200.0 / max(e0.elapsed_time(e1), 1e-3)))
-        e0.record()
-        for _ in range(reps):
+        if args.profile_once:
+            # for a profiler: one more call per kernel, no timing
             call()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        st, detail = binding.sgemm_poll_device_status(s)
+            torch.cuda.synchronize()
+            print(json.dumps({"workload": w.name, "path": path, "calls": max(3, args.warmup) + 1,
+                              "config": binding.sgemm_last_config()}), flush=True)
+            continue
+        reps = _reps_for(call, budget_ms=300.0)
+        ms, dist = _timing_fields(call, reps, flush)
         tf = gemm_flops(w.M, w.N, w.K) / ms / 1e9
-        print(json.dumps({"workload": name, "path": "ffma", "M": w.M, "N": w.N, "K": w.K,
-                          "alpha": w.alpha, "beta": w.beta, "ms": round(ms, 5),
-                          "gflops": round(tf * 1e3, 1),
-                          "pct_of_ffma_peak": round(100 * tf / peak_tf, 2),
-                          "min_bytes": min_bytes(w.M, w.N, w.K, w.beta),
-                          "achieved_min_gbs": round(min_bytes(w.M, w.N, w.K, w.beta) / ms / 1e6, 1),
-                          "reps": reps, "status": st,
-                          "config": binding.sgemm_last_config()}), flush=True)
-        # the opt-in tensor-core path, reported apart
-        def call3():
-            st3 = binding.sgemm_3xtf32(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA,
-                                       dB.data_ptr(), w.LDB, w.beta, dC.data_ptr(), w.LDC, s)
-            if st3 != 0:
-                raise RuntimeError(binding.sgemm_status_string(st3))
-        for _ in range(3):
-            call3()
-        torch.cuda.synchronize()
-        e0.record()
-        for _ in range(reps):
-            call3()
-        e1.record()
-        torch.cuda.synchronize()
-        ms3 = e0.elapsed_time(e1) / reps
-        st3, _ = binding.sgemm_poll_device_status(s)
-        tf3 = gemm_flops(w.M, w.N, w.K) / ms3 / 1e9
-        p3 = tf32x3_peak_tflops(peaks)
-        print(json.dumps({"workload": name, "path": "3xtf32", "M": w.M, "N": w.N, "K": w.K,
-                          "alpha": w.alpha, "beta": w.beta, "ms": round(ms3, 5),
-                          "gflops": round(tf3 * 1e3, 1),
-                          "pct_of_3xtf32_tensor_roof": round(100 * tf3 / p3, 2) if p3 else None,
-                          "reps": reps, "status": st3,
-                          "config": binding.sgemm_last_config()}), flush=True)
-        del dA, dB, dC
-        torch.cuda.empty_cache()
+        line = {"workload": w.name, "path": path, "M": w.M, "N": w.N, "K": w.K, "ms": round(ms, 5),
+                "gflops": round(tf * 1e3, 1), "pct_of_ffma_peak": round(100 * tf / peak_tf, 2)}
+        line.update(dist)
+        line.update({"reps": reps, "config": binding.sgemm_last_config()})
+        if k is not None and w.M == w.N == w.K == 4096:
+            line["pages_gflops_rtx5080"] = PAGES_LADDER_GFLOPS[k]
+        if path == "sgemm":
+            base_ms = ms
+        lines.append(line)
+    for line in lines if base_ms else []:
+        line["time_vs_sgemm"] = round(line["ms"] / base_ms, 2)
+        print(json.dumps(line), flush=True)
 
 
 def main(argv=None):
@@ -528,11 +620,18 @@ def main(argv=None):
                     help="skip timing the opt-in 3xTF32 tensor-core path")
     ap.add_argument("--report", action="store_true",
                     help="time every named workload and the sweep, one JSON line each")
+    ap.add_argument("--ladder", action="store_true",
+                    help="time the pages' kernels 3, 7, 8 and sgemm on --workload")
+    ap.add_argument("--profile-once", action="store_true",
+                    help="with --ladder: warm-up calls plus one call per kernel, no timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.report:
         run_report(args)
+        return
+    if args.ladder:
+        run_ladder(args)
         return
     from dense_fp32_gemm_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]

@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_3xtf32": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_ex": (I, [I, I, I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_host": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_ladder": (I, [I, I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
                                               I, P]),
             }
@@ -222,6 +223,16 @@ def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> 
     the kernel's scratch comes from a fixed buffer inside the library.
     Returns the status code."""
     return lib().sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_ladder(kernel, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """One of the pages' kernels (3: shared-memory tiling, 7: vectorized
+    block tiling, 8: warp tiling) on device matrices; same arguments and
+    result as sgemm(). Returns the status code."""
+    return lib().sgemm_ladder(kernel, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+LADDER_KERNELS = (3, 7, 8)
 
 
 # ---- torch conveniences (marshalling only) ------------------------------------------

@@ -241,6 +241,28 @@ long long sgemm_set_wait_timeout_ns(long long ns);
 int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
                   int ldb, float beta, float* C, int ldc, void* stream);
 
+/*
+ * Three kernels of the pages' series, rebuilt for this GPU to measure what
+ * each technique buys; sgemm() never uses them:
+ *   kernel 3 -- shared-memory tiling ("Shared Memory Tiling"): 32 x 32 C tile
+ *               per CTA of 1024 threads, one output per thread;
+ *   kernel 7 -- vectorized 2-D block tiling ("Vectorized Memory Access:
+ *               128-bit Loads and Stores"): 128 x 128 C tile, BK = 8, 8 x 8
+ *               outputs per thread, 128-bit loads, A transposed in shared
+ *               memory;
+ *   kernel 8 -- warp tiling ("Warp Tiling: A Third Level of Tiling"):
+ *               128 x 64 C tile, BK = 16, 64 x 32 warp tiles of 2 x 2
+ *               sub-tiles, 4 x 4 outputs per thread and sub-tile.
+ * Arguments after `kernel`, their checks, the quick returns and the result
+ * are those of sgemm(): any shape, leading dimension and 4-byte alignment
+ * (128-bit accesses are used only when A, B and C are 16-byte aligned and
+ * lda, ldb, ldc are multiples of 4). One CTA per C tile on `stream`; no
+ * workspace and no device status. kernel other than 3, 7 or 8 returns
+ * SGEMM_ERR_INVALID_VALUE; more than 2^31 - 1 tiles SGEMM_ERR_INVALID_DIM.
+ */
+int sgemm_ladder(int kernel, int M, int N, int K, float alpha, const float* A, int lda,
+                 const float* B, int ldb, float beta, float* C, int ldc, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -52,6 +52,13 @@ def test_validation_happens_before_any_device_call():
                                          None) == binding.SGEMM_ERR_INVALID_DIM
     assert binding.sgemm_strided_batched(0, 0, 4, 4, 4, 1.0, 16, 4, 16, 16, 4, 16, 0.0, 16, 4, 16, 0,
                                          None) == binding.SGEMM_OK
+    for k in binding.LADDER_KERNELS:
+        assert binding.sgemm_ladder(k, 4, -4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_DIM
+        assert binding.sgemm_ladder(k, 4, 4, 4, 1.0, 16, 4, 16, 3, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_LD
+        assert binding.sgemm_ladder(k, 4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 17, 4, None) == binding.SGEMM_ERR_MISALIGNED
+        assert binding.sgemm_ladder(k, 0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4, None) == binding.SGEMM_OK
+    for k in (0, 1, 6, 9):
+        assert binding.sgemm_ladder(k, 4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_VALUE
 
 
 def test_config_registry():
