@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_ex": (I, [I, I, I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_host": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_ladder": (I, [I, I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_3xtf32_set_cluster_size": (I, [I]),
                 "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
                                               I, P]),
             }
@@ -233,6 +234,12 @@ def sgemm_ladder(kernel, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=No
 
 
 LADDER_KERNELS = (3, 7, 8)
+
+
+def sgemm_3xtf32_set_cluster_size(cluster_size: int) -> int:
+    """2: sgemm_3xtf32 runs CTA pairs sharing B tiles by multicast (default);
+    1: single CTAs. Returns the previous setting (or an error status)."""
+    return lib().sgemm_3xtf32_set_cluster_size(cluster_size)
 
 
 # ---- torch conveniences (marshalling only) ------------------------------------------

@@ -54,6 +54,16 @@ __device__ __forceinline__ void commit(uint32_t mbar_smem) {
       : "memory");
 }
 
+// The same, arriving on the mbarrier at offset `mbar_smem` in every CTA of the
+// cluster whose bit is set in `cta_mask`.
+__device__ __forceinline__ void commit_multicast(uint32_t mbar_smem, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(mbar_smem),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // ---- TMEM -> registers: 32 lanes x 32 bits, 16 consecutive columns -------
 // Lane i of the warp receives row (lane base + i) of the addressed block.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {

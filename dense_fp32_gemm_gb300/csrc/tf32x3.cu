@@ -22,12 +22,24 @@
 //      256-column TMEM accumulator and issues, per 8-wide k-step, the three
 //      tcgen05.mma.kind::tf32 products; warps 2-5 read the accumulator back
 //      with tcgen05.ld and apply alpha * acc + beta * C.
+//
+// Cluster form (CL = 2, the default where the device can co-schedule CTA
+// pairs): the two CTAs of a cluster compute vertically adjacent tiles (tile
+// rows 2i and 2i + 1 of the same tile column) in lockstep, so they need the
+// same B tile. Each CTA loads its own A tiles and one half (128 rows) of the
+// B_hi and B_lo tiles, multicast into both CTAs' shared memory: the pair
+// reads B from L2 once instead of twice, a third less operand traffic per
+// CTA. A stage is refilled only after the MMAs of both CTAs have read it
+// (each MMA warp's commit arrives on the "empty" barrier of both CTAs), and
+// before exiting every CTA waits until its barriers have received the peer's
+// last arrivals, then meets the peer at a cluster barrier.
 // Every wait is bounded (see ffma_sgemm.cuh); a CTA that gives up drains its
 // copies and MMAs, frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -157,6 +169,7 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc
   }
 }
 
+template <int CL>
 __global__ void __launch_bounds__(NT, 1)
     gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmA_hi,
                 const __grid_constant__ CUtensorMap tmA_lo, const __grid_constant__ CUtensorMap tmB_hi,
@@ -168,15 +181,20 @@ __global__ void __launch_bounds__(NT, 1)
   volatile int* abort_w = &bar->abort;
   const uint32_t base_addr = ptx::smem_addr(base);
 
+  static_assert(CL == 1 || CL == 2, "cluster size");
+  constexpr uint16_t kPair = 0x3;  // both CTAs of a cluster of two
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Schedule& sc = p.sched;
-  const int b = blockIdx.x;
+  // the schedule hands out work per cluster; rank r takes tile row CL * i + r
+  const int rank = CL == 2 ? (int)ptx::cluster_ctarank() : 0;
+  const int b = blockIdx.x / CL;
+  const int slot = b * CL + rank;  // this CTA's partial tile and flag
   const int npieces = num_pieces(sc, b);
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bar->full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), CL);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_addr(&bar->tmem_full[i]), 1);
@@ -197,6 +215,8 @@ __global__ void __launch_bounds__(NT, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
+  // the peer's barriers must be initialised before anything is multicast to them
+  if (CL == 2) ptx::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem = bar->tmem_addr;
 
@@ -208,6 +228,7 @@ __global__ void __launch_bounds__(NT, 1)
         const Piece pc = get_piece(sc, b, i);
         int tm, tn;
         tile_coords(sc, pc.tile, tm, tn);
+        tm = tm * CL + rank;
         bool ok = true;
         for (int kb = pc.kb; kb < pc.ke; ++kb, ++it) {
           const int s = it % ST;
@@ -222,8 +243,17 @@ __global__ void __launch_bounds__(NT, 1)
           ptx::mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
           ptx::tma_load_2d(st0, &tmA_hi, kb * BK, tm * BM, fb);
           ptx::tma_load_2d(st0 + A_BYTES, &tmA_lo, kb * BK, tm * BM, fb);
-          ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB_hi, kb * BK, tn * BN, fb);
-          ptx::tma_load_2d(st0 + 2 * A_BYTES + B_BYTES, &tmB_lo, kb * BK, tn * BN, fb);
+          if (CL == 1) {
+            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB_hi, kb * BK, tn * BN, fb);
+            ptx::tma_load_2d(st0 + 2 * A_BYTES + B_BYTES, &tmB_lo, kb * BK, tn * BN, fb);
+          } else {
+            // this CTA's half of each B tile, into both CTAs
+            const uint32_t half = (uint32_t)(rank * (B_BYTES / 2));
+            const int row = tn * BN + rank * (BN / 2);
+            ptx::tma_load_2d_multicast(st0 + 2 * A_BYTES + half, &tmB_hi, kb * BK, row, fb, kPair);
+            ptx::tma_load_2d_multicast(st0 + 2 * A_BYTES + B_BYTES + half, &tmB_lo, kb * BK, row,
+                                       fb, kPair);
+          }
         }
         if (!ok) break;
       }
@@ -234,6 +264,15 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t fb = ptx::smem_addr(&bar->full[j % ST]);
         while (!ptx::mbar_try_wait(fb, (uint32_t)((j / ST) & 1)))
           if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+      }
+      if (CL == 2) {
+        // the peer's MMA warp arrives on this CTA's empty barriers: wait
+        // (bounded) for its arrivals on the last use of every stage
+        for (int j = it; j < it + ST; ++j) {
+          const uint32_t eb = ptx::smem_addr(&bar->empty[j % ST]);
+          while (!ptx::mbar_try_wait(eb, (uint32_t)((j / ST) & 1) ^ 1u))
+            if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+        }
       }
     }
   } else if (warp == 1) {
@@ -273,7 +312,11 @@ __global__ void __launch_bounds__(NT, 1)
             tc::mma_tf32(d, a_lo, b_hi, IDESC, 1u);
           }
           issued_any = true;
-          tc::commit(ptx::smem_addr(&bar->empty[s]));  // frees the stage when done
+          // frees the stage (in both CTAs of a pair) once these MMAs are done
+          if (CL == 1)
+            tc::commit(ptx::smem_addr(&bar->empty[s]));
+          else
+            tc::commit_multicast(ptx::smem_addr(&bar->empty[s]), kPair);
         }
         if (!ok) break;
         tc::commit(ptx::smem_addr(&bar->tmem_full[buf]));  // the piece's accumulator is ready
@@ -308,7 +351,7 @@ __global__ void __launch_bounds__(NT, 1)
                                    abort_w, p.status, kDevTimeoutFull, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after_sync();
-      float* my_ws = p.ws + (long long)b * (BM * BN);
+      float* my_ws = p.ws + (long long)slot * (BM * BN);
       if (is_partial_piece(sc, pc)) {
         // publish the partial tile (column-major: a warp writes 128 bytes
         // per column)
@@ -323,14 +366,14 @@ __global__ void __launch_bounds__(NT, 1)
         if (!epi_sync()) break;
         if (warp == 2 && lane == 0) {
           __threadfence();
-          ptx::st_release(p.flags + b, p.epoch);
+          ptx::st_release(p.flags + slot, p.epoch);
         }
       } else {
         const int nc = num_contributors(sc, b, pc);
         if (nc > 0) {
           if (warp == 2 && lane == 0) {
             for (int c = 1; c <= nc && !*abort_w; ++c) {
-              const uint32_t* f = p.flags + b + c;
+              const uint32_t* f = p.flags + (b + c) * CL + rank;
               const uint64_t t0 = ptx::global_ns();
               while (ptx::ld_acquire(f) != p.epoch) {
                 if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) {
@@ -346,6 +389,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         int tm, tn;
         tile_coords(sc, pc.tile, tm, tn);
+        tm = tm * CL + rank;
         const int row = tm * BM + r;
         const bool row_ok = row < p.M;
         float* crow = p.C + (long long)(row_ok ? row : 0) * p.ldc;
@@ -357,9 +401,9 @@ __global__ void __launch_bounds__(NT, 1)
           float a[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) a[e] = __uint_as_float(v[e]);
-          // partials of CTAs b+1 .. b+nc, in that order
+          // partials of schedule units b+1 .. b+nc (same rank), in that order
           for (int c = 1; c <= nc; ++c) {
-            const float* src = my_ws + (long long)c * (BM * BN);
+            const float* src = p.ws + (long long)((b + c) * CL + rank) * (BM * BN);
 #pragma unroll
             for (int e = 0; e < 16; ++e) a[e] += __ldcg(src + (c0 + e) * BM + r);
           }
@@ -402,11 +446,16 @@ __global__ void __launch_bounds__(NT, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }
+  // neither CTA of a pair leaves while the other may still write to it
+  if (CL == 2) ptx::cluster_sync();
 }
 
-// Per-device set-up (shared-memory attribute), guarded by g_mutex.
+// Per-device set-up (shared-memory attributes, how many CTA pairs can be
+// resident at once), guarded by g_mutex.
 std::mutex g_mutex;
 bool g_ready[64];
+int g_pairs[64];          // resident clusters of two; 0 = the pair form cannot run
+std::atomic<int> g_cluster_size{2};  // 2: the pair form where possible; 1: single CTAs
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_tried = false;
 
@@ -469,18 +518,42 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
   }
 
+  int pairs = 0;
   {
     std::lock_guard<std::mutex> lock(x3::g_mutex);
     if (dev < 0 || dev >= 64) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     if (!x3::g_ready[dev]) {
-      if (cudaFuncSetAttribute(x3::gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(x3::gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               x3::SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(x3::gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                x3::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
       }
+      // how many clusters of two fit at once (SMs pair up within a GPC, so
+      // this can be below sms / 2)
+      cudaLaunchConfig_t qc = {};
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 2;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.gridDim = dim3(2 * (unsigned)(sms / 2 > 0 ? sms / 2 : 1));
+      qc.blockDim = dim3(x3::NT);
+      qc.dynamicSmemBytes = x3::SMEM_BYTES;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, x3::gemm_kernel<2>, &qc) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      x3::g_pairs[dev] = n;
       x3::g_ready[dev] = true;
     }
+    pairs = x3::g_pairs[dev];
   }
+  int CL = (x3::g_cluster_size.load() == 2 && pairs > 0) ? 2 : 1;
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   {
     std::lock_guard<std::mutex> lock(x3::g_mutex);
@@ -488,22 +561,31 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   }
   if (enc == nullptr) return SGEMM_ERR_LAUNCH;
 
-  // schedule: whole tiles, then the last one to two waves split along K
+  // schedule: whole tiles, then the last one to two waves split along K. In
+  // the pair form a schedule unit is two vertically adjacent tiles (a tile row
+  // pair), handed to one cluster.
   const int tiles_m = (M + x3::BM - 1) / x3::BM, tiles_n = (N + x3::BN - 1) / x3::BN;
   const int kiters = (K + x3::BK - 1) / x3::BK;
-  const Schedule sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, 2);
+  Schedule sched = make_schedule((tiles_m + 1) / 2, tiles_n, kiters, pairs, 4, 2);
+  if (CL == 2 && sched.dp_tiles == 0) {
+    // every tile is split along K: the pairs' lockstep costs more than the
+    // shared B tiles save (measured at 1024^3, 2048^3 and 16384 x 64 x 4096)
+    CL = 1;
+  }
+  if (CL == 1) sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, 2);
   const bool split = sched.dp_tiles < sched.tiles;
+  const int ctas = sched.grid * CL;
 
   // workspace: A_hi, A_lo (M x Kp), B_hi, B_lo transposed (N x Kp), then one
   // partial tile per CTA when the schedule splits
   const long long Kp = ((long long)K + 3) / 4 * 4;
   const size_t split_floats = (size_t)(2 * (long long)M * Kp + 2 * (long long)N * Kp);
-  const size_t partial_floats = split ? (size_t)sched.grid * x3::BM * x3::BN : 0;
+  const size_t partial_floats = split ? (size_t)ctas * x3::BM * x3::BN : 0;
   float* ws = nullptr;
   int* status = nullptr;
   uint32_t* flags = nullptr;
   uint32_t epoch = 0;
-  st = library_workspace(dev, stream, split_floats + partial_floats, (size_t)sched.grid, &ws, &status,
+  st = library_workspace(dev, stream, split_floats + partial_floats, (size_t)ctas, &ws, &status,
                          &flags, &epoch);
   if (st != SGEMM_OK) return st;
   float* a_hi = ws;
@@ -528,8 +610,8 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   CUtensorMap mA_hi, mA_lo, mB_hi, mB_lo;
   if (!x3::encode_k_major(enc, &mA_hi, a_hi, M, K, Kp, x3::BM) ||
       !x3::encode_k_major(enc, &mA_lo, a_lo, M, K, Kp, x3::BM) ||
-      !x3::encode_k_major(enc, &mB_hi, b_hi, N, K, Kp, x3::BN) ||
-      !x3::encode_k_major(enc, &mB_lo, b_lo, N, K, Kp, x3::BN))
+      !x3::encode_k_major(enc, &mB_hi, b_hi, N, K, Kp, x3::BN / CL) ||
+      !x3::encode_k_major(enc, &mB_lo, b_lo, N, K, Kp, x3::BN / CL))
     return SGEMM_ERR_LAUNCH;
   x3::Params p;
   p.M = M;
@@ -545,12 +627,38 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   p.epoch = epoch;
   p.status = status;
   p.timeout_ns = library_wait_timeout_ns();
-  x3::gemm_kernel<<<p.sched.grid, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi, mB_lo);
-  if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  if (CL == 1) {
+    x3::gemm_kernel<1><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi, mB_lo);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  } else {
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = 2;
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    lc.gridDim = dim3((unsigned)ctas);
+    lc.blockDim = dim3(x3::NT);
+    lc.dynamicSmemBytes = x3::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = la;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, x3::gemm_kernel<2>, p, mA_hi, mA_lo, mB_hi, mB_lo) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+  }
   char text[160];
-  snprintf(text, sizeof(text), "3xtf32_tcgen05_%dx%dx%d_s%d grid=%d dp=%d split=%d kiters=%d",
-           x3::BM, x3::BN, x3::BK, x3::ST, sched.grid, sched.dp_tiles,
+  snprintf(text, sizeof(text),
+           "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d grid=%d units=%d dp=%d split=%d kiters=%d",
+           x3::BM, x3::BN, x3::BK, x3::ST, CL, ctas, sched.grid, sched.dp_tiles,
            sched.tiles - sched.dp_tiles, kiters);
   note_last_config(text);
   return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_3xtf32_set_cluster_size(int cluster_size) {
+  if (cluster_size != 1 && cluster_size != 2) return SGEMM_ERR_INVALID_VALUE;
+  return x3::g_cluster_size.exchange(cluster_size);
 }

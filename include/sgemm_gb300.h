@@ -87,6 +87,17 @@ int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, cons
                  int ldb, float beta, float* C, int ldc, void* stream);
 
 /*
+ * Kernel form of sgemm_3xtf32 for later calls (process-wide): 2 (the default)
+ * runs clusters of two CTAs on vertically adjacent tiles that share each B
+ * tile through TMA multicast, where the device can co-schedule CTA pairs and
+ * the problem has at least two waves of whole tile pairs (else single CTAs);
+ * 1 always runs single CTAs, each loading its own B tiles. Both give the
+ * same results within the tolerance (bit-identical on integer inputs). Returns the previous setting, or
+ * SGEMM_ERR_INVALID_VALUE (nothing changed) for another value.
+ */
+int sgemm_3xtf32_set_cluster_size(int cluster_size);
+
+/*
  * C = alpha * op(A) * op(B) + beta * C, row-major, FFMA path. op(A) is M x K:
  * A itself (SGEMM_OP_N, stored M x K, lda >= max(1, K)) or the transpose of an
  * A stored K x M (SGEMM_OP_T, lda >= max(1, M)); op(B) is K x N: B (stored

@@ -1,7 +1,9 @@
 """The opt-in tensor-core path (sgemm_3xtf32) against the oracle: the same
 bar as the FFMA path -- bit-exact on integer inputs, the FP32 tolerance
 |C - C_ref| <= 1e-5 * (|alpha| sum |a||b| + |beta| |c|) + 1e-30 on real inputs --
-on small shapes element by element and on the full workloads by sampling."""
+on small shapes element by element and on the full workloads by sampling.
+Every test runs in both kernel forms: CTA pairs sharing B tiles by multicast
+(the default) and single CTAs."""
 import numpy as np
 import pytest
 import torch
@@ -13,6 +15,23 @@ import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
 X3 = binding.sgemm_3xtf32
+
+
+@pytest.fixture(autouse=True, params=[2, 1], ids=["pairs", "single"])
+def cluster_size(request):
+    prev = binding.sgemm_3xtf32_set_cluster_size(request.param)
+    yield request.param
+    binding.sgemm_3xtf32_set_cluster_size(prev)
+
+
+def test_kernel_form_is_reported(cluster_size):
+    # two waves of whole tile pairs: the pair form runs when selected
+    w = Workload("x3form", 128 * 2 * 76 * 2, 256, 64, 1.0, 0.0, "int3", 36)
+    H.check_sampled(w, rows=64, elements=4096, fn=X3)
+    assert f"cluster={cluster_size}" in binding.sgemm_last_config()
+    # every tile split along K: single CTAs either way
+    H.check_against_oracle(Workload("x3split", 300, 520, 4000, 1.0, 0.0, "int3", 37), fn=X3)
+    assert "cluster=1" in binding.sgemm_last_config()
 
 SHAPES = [(128, 256, 32), (1, 1, 1), (7, 9, 3), (33, 65, 17), (257, 129, 100), (300, 520, 77),
           (129, 257, 1000), (513, 1031, 40), (64, 64, 4097), (2, 700, 2049), (1000, 40, 129)]
