@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_host": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_ladder": (I, [I, I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_3xtf32_set_cluster_size": (I, [I]),
+                "sgemm_host_set_pipeline": (I, [I, I, I, I]),
                 "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
                                               I, P]),
             }
@@ -107,6 +108,12 @@ def sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int
     """C = alpha*A*B + beta*C on HOST matrices (addresses as ints), copies
     overlapped with the GEMM; C is final once `stream` is synchronised."""
     return lib().sgemm_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_host_set_pipeline(first: int, mid: int, last: int, panels: int) -> int:
+    """K-chunk widths (first, middle, last) and the row panels of the last
+    chunk for later sgemm_host calls; 0 picks the default. Returns a status."""
+    return lib().sgemm_host_set_pipeline(first, mid, last, panels)
 
 
 def sgemm_ex(opA, opB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

@@ -31,7 +31,39 @@ int library_device_sms(int dev, int* sms);
 namespace {
 
 constexpr int kMaxChunks = 9;
-constexpr int kMaxPanels = 4;
+constexpr int kMaxPanels = 8;
+
+// The copy/compute pipeline: K chunk widths and the row panels of the last
+// chunk (sgemm_host_set_pipeline). Widths are rounded up to multiples of 32.
+struct Pipeline {
+  int first = 256;   // first chunk (only when K >= 2 * first + last)
+  int mid = 1024;    // target width of the chunks between the first and the last
+  int last = 0;      // last chunk; 0: as wide as the middle chunks
+  int panels = 4;    // row panels of the last chunk (only when M >= 512 * panels)
+};
+Pipeline g_pipe;
+
+// Chunk boundaries 0 = kb[0] < ... < kb[n] = K for a K-wide problem.
+int chunk_bounds(int K, const Pipeline& pp, int* kb) {
+  auto r32 = [](int x) { return (x + 31) / 32 * 32; };
+  const int first = r32(pp.first), last = pp.last > 0 ? r32(pp.last) : 0;
+  int n = 0;
+  kb[n++] = 0;
+  int k_lo = 0, k_hi = K;
+  if (first > 0 && K >= 2 * first + last) {
+    kb[n++] = first;
+    k_lo = first;
+  }
+  if (last > 0 && k_hi - last > k_lo) k_hi -= last;
+  int parts = (k_hi - k_lo) / (pp.mid > 32 ? pp.mid : 32);
+  const int room = kMaxChunks - (n - 1) - (k_hi < K ? 1 : 0);
+  parts = parts < 1 ? 1 : (parts > room ? room : parts);
+  const int step = r32((k_hi - k_lo + parts - 1) / parts);
+  for (int k = k_lo + step; k < k_hi; k += step) kb[n++] = k;
+  if (k_hi < K) kb[n++] = k_hi;
+  kb[n] = K;
+  return n;
+}
 
 struct HostCtx {
   bool ready = false;
@@ -194,21 +226,10 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
         (st = grow(&c->dB, &c->capB, (size_t)K * N)) != SGEMM_OK)
       return st;
     if (beta != 0.f && (st = grow(&c->dC0, &c->capC0, mn)) != SGEMM_OK) return st;
-    // K chunk boundaries: a narrow first chunk (256) when K is large, then
-    // equal chunks of at least 512 (multiples of 32), at most kMaxChunks in all
-    int kb[kMaxChunks + 1];
-    int nk = 0;
-    kb[nk++] = 0;
-    int k_rest = 0;
-    if (K >= 2048) {
-      kb[nk++] = 256;
-      k_rest = 256;
-    }
-    int parts = (K - k_rest) / 1024;
-    parts = parts < 1 ? 1 : (parts > kMaxChunks - 1 ? kMaxChunks - 1 : parts);
-    const int step = ((K - k_rest + parts - 1) / parts + 31) / 32 * 32;
-    for (int k = k_rest + step; k < K; k += step) kb[nk++] = k;
-    kb[nk] = K;
+    // K chunk boundaries: a narrow first chunk, equal middle chunks, and a
+    // last chunk that is computed (and copied back) in row panels
+    int kb[kMaxChunks + 2];
+    const int nk = chunk_bounds(K, g_pipe, kb);
     for (int i = 0; i < nk; ++i) {
       const int k0 = kb[i], k1 = kb[i + 1];
       if (cudaMemcpy2DAsync(c->dA + k0, (size_t)K * 4, A + k0, (size_t)lda * 4,
@@ -232,7 +253,7 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
     }
     // last chunk in row panels, each copied back as soon as it is final
     const int k0 = kb[nk - 1], kl = K - k0;
-    const int panels = M >= 2048 ? kMaxPanels : 1;
+    const int panels = M >= 512 * g_pipe.panels ? g_pipe.panels : (M >= 1024 ? M / 512 : 1);
     const int rows = ((M + panels - 1) / panels + 127) / 128 * 128;
     if (cudaStreamWaitEvent(user, c->chunk[nk - 1], 0) != cudaSuccess) return fail();
     if (beta != 0.f && cudaStreamWaitEvent(user, c->c_in, 0) != cudaSuccess) return fail();
@@ -267,5 +288,17 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
       cudaEventRecord(c->out, c->d2h) != cudaSuccess ||
       cudaStreamWaitEvent(user, c->out, 0) != cudaSuccess)
     return fail();
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_host_set_pipeline(int first, int mid, int last, int panels) {
+  if (first < 0 || mid < 0 || last < 0 || panels < 0 || panels > kMaxPanels)
+    return SGEMM_ERR_INVALID_VALUE;
+  std::lock_guard<std::mutex> lock(g_host_mutex);
+  const Pipeline defaults;
+  g_pipe.first = first;
+  g_pipe.mid = mid > 0 ? mid : defaults.mid;
+  g_pipe.last = last;
+  g_pipe.panels = panels > 0 ? panels : defaults.panels;
   return SGEMM_OK;
 }

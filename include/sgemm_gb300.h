@@ -140,6 +140,19 @@ int sgemm_strided_batched(int opA, int opB, int M, int N, int K, float alpha, co
 int sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
                float beta, float* C, int ldc, void* stream);
 
+/*
+ * Copy/compute pipeline of later sgemm_host calls (process-wide): K is cut
+ * into a first chunk of `first` columns (0: none; taken only when K >= 2 *
+ * first + last), middle chunks of about `mid` columns (0: 1024), and a last
+ * chunk of `last` columns (0: as wide as the middle chunks) that is computed
+ * and copied back in `panels` row panels (0: 4; at most 8; fewer when M <
+ * 512 * panels). Widths are rounded up to multiples of 32; at most 9 chunks.
+ * The result does not depend on the setting beyond the order of the sum
+ * over k. Returns SGEMM_ERR_INVALID_VALUE (nothing changed) for a negative
+ * value or more than 8 panels.
+ */
+int sgemm_host_set_pipeline(int first, int mid, int last, int panels);
+
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* sgemm_status_string(int status);
 

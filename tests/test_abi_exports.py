@@ -61,6 +61,8 @@ def test_validation_happens_before_any_device_call():
     assert binding.sgemm_3xtf32_set_cluster_size(0) == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_3xtf32_set_cluster_size(1) == 2
     assert binding.sgemm_3xtf32_set_cluster_size(2) == 1
+    assert binding.sgemm_host_set_pipeline(-1, 0, 0, 0) == binding.SGEMM_ERR_INVALID_VALUE
+    assert binding.sgemm_host_set_pipeline(0, 0, 0, 9) == binding.SGEMM_ERR_INVALID_VALUE
     for k in (0, 1, 6, 9):
         assert binding.sgemm_ladder(k, 4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_VALUE
 

@@ -68,3 +68,15 @@ def test_host_full_size_integer():
                               w.beta, hC.data_ptr(), w.N, s.cuda_stream) == 0
     s.synchronize()
     H.freivalds(w, A, B, C, hC.numpy().reshape(w.M, w.N))
+
+
+@pytest.mark.parametrize("pipeline", [(128, 512, 256, 8), (0, 4096, 0, 1), (256, 1024, 512, 2),
+                                      (64, 64, 64, 3)], ids=lambda p: "-".join(map(str, p)))
+def test_host_pipeline_settings(pipeline):
+    # any chunking of K and any panel count give the same (exact) result
+    assert binding.sgemm_host_set_pipeline(*pipeline) == 0
+    try:
+        _host_call(Workload("hostpipe", 2100, 300, 3000, 1.25, -0.5, "int3", 88))
+        _host_call(Workload("hostpipe", 2100, 300, 3000, 1.25, -0.5, "uniform", 89))
+    finally:
+        assert binding.sgemm_host_set_pipeline(0, 0, 0, 0) == 0
