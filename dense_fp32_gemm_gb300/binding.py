@@ -26,6 +26,7 @@ SGEMM_ERR_ALLOC = -7
 SGEMM_ERR_MISALIGNED = -8
 SGEMM_ERR_INVALID_VALUE = -9
 SGEMM_ERR_NOALLOC_CAPACITY = -10
+SGEMM_ERR_CAPTURE = -11
 
 SGEMM_OP_N = 0
 SGEMM_OP_T = 1

@@ -109,6 +109,14 @@ int get_workspace(int dev, cudaStream_t stream, size_t flags, size_t partial_flo
                   Workspace** out) {
   Workspace& w = g_workspaces[{dev, stream}];
   if (w.block == nullptr || w.flag_cap < flags || w.partial_cap < partial_floats) {
+    // allocation is not allowed while the stream is captured into a graph:
+    // refuse instead of invalidating the capture
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_CAPTURE;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return SGEMM_ERR_CAPTURE;
     const size_t fcap = flags > w.flag_cap ? flags : w.flag_cap;
     const size_t pcap = partial_floats > w.partial_cap ? partial_floats : w.partial_cap;
     const size_t status_bytes = 256;
@@ -383,6 +391,8 @@ SGEMM_API const char* sgemm_status_string(int status) {
     case SGEMM_ERR_INVALID_VALUE: return "invalid argument value";
     case SGEMM_ERR_NOALLOC_CAPACITY:
       return "problem needs more scratch than the fixed no-allocation buffer holds";
+    case SGEMM_ERR_CAPTURE:
+      return "workspace must grow while the stream is being captured (call once before capture)";
     default: return "unknown status";
   }
 }
@@ -440,6 +450,10 @@ SGEMM_API int sgemm_poll_device_status(void* stream_, int* detail) {
     return SGEMM_ERR_LAUNCH;
   if (code != 0) {
     if (cudaMemset(it->second.status, 0, sizeof(int)) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    // an aborted launch can leave split-K flags set that no owner consumed
+    if (it->second.flags != nullptr &&
+        cudaMemset(it->second.flags, 0, it->second.flag_cap * 4) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
     if (detail) *detail = code;
     return SGEMM_ERR_DEVICE_TIMEOUT;
   }

@@ -71,7 +71,8 @@ struct KernelParams {
   long long sA, sB, sC; // elements between consecutive matrices of a batch
   Schedule sched;
   float* ws;            // grid * BM * BN floats: one partial tile per CTA
-  uint32_t* flags;      // grid flags: flags[b] == epoch once slot b is written
+  uint32_t* flags;      // grid flags: flags[b] == epoch once slot b is written; the
+                        // owner of the tile resets it to 0 after reading the slot
   int* status;          // device status word
   uint32_t epoch;       // value of a flag published by this launch
   int c_vec;            // C is 16-byte aligned and ldc % 4 == 0
@@ -562,18 +563,22 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
       if (nc > 0) {
         if (tid == 0) {
           for (int c = 1; c <= nc; ++c) {
-            const uint32_t* f = p.flags + b + c;
-            if (ptx::ld_acquire(f) == p.epoch) continue;
-            const uint64_t t0 = ptx::global_ns();
-            while (ptx::ld_acquire(f) != p.epoch) {
-              if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) {
-                *abort_w = 1;
-                atomicCAS(p.status, 0, (int)kDevTimeoutFlag);
-                break;
+            uint32_t* f = p.flags + b + c;
+            if (ptx::ld_acquire(f) != p.epoch) {
+              const uint64_t t0 = ptx::global_ns();
+              while (ptx::ld_acquire(f) != p.epoch) {
+                if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) {
+                  *abort_w = 1;
+                  atomicCAS(p.status, 0, (int)kDevTimeoutFlag);
+                  break;
+                }
+                __nanosleep(200);
               }
-              __nanosleep(200);
             }
             if (*abort_w) break;
+            // consumed: no later launch can mistake it for its own, even one
+            // that reuses this epoch (a CUDA graph replays its arguments)
+            *f = 0u;
           }
         }
         if (!cta_sync() || *abort_w) {

@@ -93,7 +93,8 @@ struct Params {
   long long ldc;
   Schedule sched;     // whole tiles, then K-split tiles (schedule.hpp)
   float* ws;          // grid partial tiles of BM x BN floats, column-major
-  uint32_t* flags;    // flags[b] == epoch once CTA b's partial is written
+  uint32_t* flags;    // flags[s] == epoch once slot s's partial is written; reset
+                      // to 0 by the owner that reads it
   uint32_t epoch;
   int* status;
   long long timeout_ns;
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (nc > 0) {
           if (warp == 2 && lane == 0) {
             for (int c = 1; c <= nc && !*abort_w; ++c) {
-              const uint32_t* f = p.flags + (b + c) * CL + rank;
+              uint32_t* f = p.flags + (b + c) * CL + rank;
               const uint64_t t0 = ptx::global_ns();
               while (ptx::ld_acquire(f) != p.epoch) {
                 if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) {
@@ -383,6 +384,9 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 __nanosleep(200);
               }
+              // consumed: a later launch (or graph replay, which reuses this
+              // epoch) never mistakes it for its own
+              if (!*abort_w) *f = 0u;
             }
           }
           if (!epi_sync() || *abort_w) break;

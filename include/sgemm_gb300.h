@@ -30,6 +30,14 @@
  * Threading: calls are asynchronous with respect to the host and ordered on
  * `stream`; the workspace is per (device, stream), so concurrent calls on
  * different streams do not share it. Host-side state is guarded by a mutex.
+ *
+ * CUDA graphs: sgemm, sgemm_ex, sgemm_strided_batched and sgemm_3xtf32 can be
+ * captured into a graph and replayed, once a call of at least the same size
+ * has run on the capturing stream outside the capture (it sets the device up
+ * and sizes the stream's workspace; a call that would have to grow it during
+ * capture returns SGEMM_ERR_CAPTURE and launches nothing). The graph keeps
+ * the stream's workspace: do not replay it concurrently with other work on
+ * that stream's workspace. sgemm_noalloc needs no workspace at all.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -49,8 +57,12 @@ typedef enum {
   SGEMM_ERR_ALLOC = -7,             /* workspace allocation failed                */
   SGEMM_ERR_MISALIGNED = -8,        /* a matrix pointer is not 4-byte aligned     */
   SGEMM_ERR_INVALID_VALUE = -9,     /* other invalid argument (config id, buffer) */
-  SGEMM_ERR_NOALLOC_CAPACITY = -10  /* sgemm_noalloc: problem needs more scratch
+  SGEMM_ERR_NOALLOC_CAPACITY = -10, /* sgemm_noalloc: problem needs more scratch
                                        than its fixed buffer holds             */
+  SGEMM_ERR_CAPTURE = -11           /* the per-stream workspace would have to grow
+                                       while `stream` is captured into a CUDA
+                                       graph (nothing launched; call once on
+                                       the stream before capturing)            */
 } sgemm_status;
 
 /* Operand forms of sgemm_ex / sgemm_strided_batched (row-major storage). */

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(0, -11, -1):
+    for code in range(0, -12, -1):
         assert binding.sgemm_status_string(code) not in ("", "unknown status")
     assert binding.sgemm_status_string(12345) == "unknown status"
 
