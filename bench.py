@@ -77,13 +77,20 @@ def tf32x3_peak_tflops(peaks):
     return (float(bf16) * TF32_OVER_BF16 / 3.0) if bf16 else None
 
 
+# The sources that define the FFMA kernel the bench times and how it is
+# configured (the other entry points and the C-ABI dispatch are left out).
+FFMA_KERNEL_SOURCES = ("ffma_sgemm.cuh", "ptx.cuh", "schedule.hpp", "tile_config.hpp",
+                       "configs.hpp", "launch.cuh", "dispatch.hpp", "tuned_table.inc", "cfg_*.cu")
+
+
 def kernel_source_hash():
-    """Hash of the sources that define the GEMM kernels (the C-ABI file,
-    which only validates and dispatches, is left out)."""
+    """Hash of the FFMA kernel's sources: a stored ncu traffic figure is used
+    only while this is unchanged."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_gemm_gb300", "csrc", "*"))):
-        if os.path.basename(f) == "api.cu":
-            continue
+    files = set()
+    for pat in FFMA_KERNEL_SOURCES:
+        files.update(glob.glob(os.path.join(ROOT, "dense_fp32_gemm_gb300", "csrc", pat)))
+    for f in sorted(files):
         h.update(os.path.basename(f).encode())
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]

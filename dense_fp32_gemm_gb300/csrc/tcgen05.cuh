@@ -80,21 +80,25 @@ __device__ __forceinline__ void tmem_wait_ld() {
 }
 
 // ---- shared-memory matrix descriptor ---------------------------------------
-// For a K-major operand tile written by TMA with 128-byte swizzle: rows of
-// 128 bytes (32 TF32 values along K), 8-row swizzle atoms of 1024 bytes laid
-// out one after another along M (or N). Fields: start address >> 4 (bits
-// 0-13), leading byte offset >> 4 (16-29, unused for this layout), stride byte
-// offset >> 4 (32-45: 1024 bytes between 8-row groups), descriptor version 1
-// (46-47), base offset 0 (49-51, the tile is 1024-byte aligned), layout type
-// 2 = 128-byte swizzle (61-63). Moving along K inside the 128-byte row is done
-// by advancing the start address (32 bytes per 8-wide k-step).
-__device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr) {
+// For a K-major operand tile written by TMA with a ROW_BYTES-byte swizzle
+// (128: 32 TF32 values along K per row; 64: 16 values; 32: 8): 8-row swizzle atoms
+// of 8 * ROW_BYTES bytes laid out one after another along M (or N). Fields:
+// start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29, unused for
+// these layouts), stride byte offset >> 4 (32-45: one atom between 8-row
+// groups), descriptor version 1 (46-47), base offset 0 (49-51, the tile
+// starts on an atom boundary), layout type (61-63: 2 = 128-byte swizzle,
+// 4 = 64-byte swizzle, 6 = 32-byte swizzle). Moving along K inside a row is done by advancing the
+// start address (32 bytes per 8-wide k-step).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t smem_desc_k_swizzled(uint32_t smem_addr) {
+  static_assert(ROW_BYTES == 128 || ROW_BYTES == 64 || ROW_BYTES == 32, "swizzle width");
+  constexpr uint64_t kLayout = ROW_BYTES == 128 ? 2u : (ROW_BYTES == 64 ? 4u : 6u);
   uint64_t d = 0;
   d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
   d |= (uint64_t)(1u) << 16;                  // leading byte offset (16 B), ignored here
-  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)(((8u * ROW_BYTES) >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1u << 46;                    // descriptor version
-  d |= (uint64_t)2u << 61;                    // 128-byte swizzle
+  d |= kLayout << 61;
   return d;
 }
 

@@ -64,10 +64,29 @@ long long library_wait_timeout_ns();
 
 namespace x3 {
 
-constexpr int BM = 128, BN = 256, BK = 32, ST = 2, NT = 192;
-constexpr int A_BYTES = BM * BK * 4;                      // 16 KB
-constexpr int B_BYTES = BN * BK * 4;                      // 32 KB
-constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 KB
+constexpr int BM = 128, BN = 256, NT = 192;
+
+// The k-slice: BK values of K per stage, in swizzled rows of 4 * BK bytes,
+// with as many stages as fit in 192 KB. BK = 16 (four 48 KB stages, 64-byte
+// swizzle) lets the loads run three stages ahead of the MMAs; BK = 32 (two
+// 96 KB stages, 128-byte swizzle) has half the per-stage hand-offs. Measured
+// on GB300: 16 is faster from K = 1024 up (4096^3: 251 against 226 TFLOP/s),
+// 32 below (8191 x 1000 x 777: 99 against 86 TFLOP/s).
+template <int BK_>
+struct Slice {
+  static constexpr int BK = BK_;
+  static_assert(BK == 32 || BK == 16, "k-slice width");
+  static constexpr int ROW_BYTES = BK * 4;
+  static constexpr int ST = 64 / BK;
+  static constexpr int A_BYTES = BM * BK * 4;                      // one of A_hi, A_lo
+  static constexpr int B_BYTES = BN * BK * 4;                      // one of B_hi, B_lo
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 or 48 KB
+};
+constexpr int kMaxStages = 4;
+constexpr int kStageRegion = 192 * 1024;
+static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
+                  Slice<32>::ST * Slice<32>::STAGE_BYTES == kStageRegion,
+              "both widths fill the same stage region");
 constexpr int ACC_COLS = BN;              // one FP32 accumulator: 128 lanes x BN columns
 constexpr int TMEM_COLS = 2 * ACC_COLS;   // two, so the epilogue overlaps the next MMAs
 constexpr int EPI_THREADS = 128;          // warps 2-5
@@ -75,8 +94,8 @@ constexpr uint32_t IDESC = tc::idesc_tf32(BM, BN);
 static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
 
 struct Barriers {
-  uint64_t full[ST];       // TMA transaction bytes of one stage
-  uint64_t empty[ST];      // MMAs that read a stage have completed
+  uint64_t full[kMaxStages];   // TMA transaction bytes of one stage
+  uint64_t empty[kMaxStages];  // MMAs that read a stage have completed
   uint64_t tmem_full[2];   // a piece's last MMA into accumulator i has completed
   uint64_t tmem_empty[2];  // the epilogue warps have read accumulator i
   uint64_t drain;          // final MMA completion on the abort path
@@ -84,7 +103,13 @@ struct Barriers {
   uint32_t tmem_addr;
   int abort;
 };
-constexpr int SMEM_BYTES = 1024 + ST * STAGE_BYTES + (int)sizeof(Barriers);
+// epilogue staging: per epilogue warp 32 rows x 32 columns (pitch 36 floats:
+// row-wise 128-bit writes and the transposed 128-bit reads are conflict-free)
+constexpr int EPI_PITCH = 36;
+constexpr int EPI_WARP_FLOATS = 32 * EPI_PITCH;
+constexpr int BAR_BYTES = ((int)sizeof(Barriers) + 15) / 16 * 16;
+constexpr int SMEM_BYTES = 1024 + kStageRegion + BAR_BYTES + 4 * EPI_WARP_FLOATS * 4;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
   int M, N, K;
@@ -170,7 +195,7 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc
   }
 }
 
-template <int CL>
+template <int CL, int BK>
 __global__ void __launch_bounds__(NT, 1)
     gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmA_hi,
                 const __grid_constant__ CUtensorMap tmA_lo, const __grid_constant__ CUtensorMap tmB_hi,
@@ -178,11 +203,15 @@ __global__ void __launch_bounds__(NT, 1)
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  Barriers* bar = reinterpret_cast<Barriers*>(base + ST * STAGE_BYTES);
+  Barriers* bar = reinterpret_cast<Barriers*>(base + kStageRegion);
+  float* epi = reinterpret_cast<float*>(base + kStageRegion + BAR_BYTES);
   volatile int* abort_w = &bar->abort;
   const uint32_t base_addr = ptx::smem_addr(base);
 
   static_assert(CL == 1 || CL == 2, "cluster size");
+  using S = Slice<BK>;
+  constexpr int ST = S::ST, ROW_BYTES = S::ROW_BYTES;
+  constexpr int A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES, STAGE_BYTES = S::STAGE_BYTES;
   constexpr uint16_t kPair = 0x3;  // both CTAs of a cluster of two
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Schedule& sc = p.sched;
@@ -303,10 +332,11 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 8; ++kk) {
             const uint32_t koff = (uint32_t)(kk * 32);  // 8 TF32 values = 32 bytes
-            const uint64_t a_hi = tc::smem_desc_k_sw128(st0 + koff);
-            const uint64_t a_lo = tc::smem_desc_k_sw128(st0 + A_BYTES + koff);
-            const uint64_t b_hi = tc::smem_desc_k_sw128(st0 + 2 * A_BYTES + koff);
-            const uint64_t b_lo = tc::smem_desc_k_sw128(st0 + 2 * A_BYTES + B_BYTES + koff);
+            const uint64_t a_hi = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + koff);
+            const uint64_t a_lo = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + A_BYTES + koff);
+            const uint64_t b_hi = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + 2 * A_BYTES + koff);
+            const uint64_t b_lo =
+                tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + 2 * A_BYTES + B_BYTES + koff);
             const uint32_t first = (kb == pc.kb && kk == 0) ? 0u : 1u;
             tc::mma_tf32(d, a_hi, b_hi, IDESC, first);
             tc::mma_tf32(d, a_hi, b_lo, IDESC, 1u);
@@ -394,46 +424,74 @@ __global__ void __launch_bounds__(NT, 1)
         int tm, tn;
         tile_coords(sc, pc.tile, tm, tn);
         tm = tm * CL + rank;
-        const int row = tm * BM + r;
-        const bool row_ok = row < p.M;
-        float* crow = p.C + (long long)(row_ok ? row : 0) * p.ldc;
+        // 32 columns at a time: lane = row while reading TMEM and the
+        // (column-major) partials, then through the warp's staging block so
+        // that the C accesses are row segments of 128 bytes: 8 lanes per row,
+        // 4 rows per access, 8 accesses for the warp's 32 rows
+        float* stage = epi + quarter * EPI_WARP_FLOATS;
+        const int sub_r = lane >> 3, sub_c = (lane & 7) * 4;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t v[16];
-          tc::tmem_ld16(acc + (uint32_t)c0, v);
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld16(acc + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+          tc::tmem_ld16(acc + (uint32_t)(c0 + 16), *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
           tc::tmem_wait_ld();
-          float a[16];
+          float a[32];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) a[e] = __uint_as_float(v[e]);
+          for (int e = 0; e < 32; ++e) a[e] = __uint_as_float(v[e]);
           // partials of schedule units b+1 .. b+nc (same rank), in that order
           for (int c = 1; c <= nc; ++c) {
             const float* src = p.ws + (long long)((b + c) * CL + rank) * (BM * BN);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) a[e] += __ldcg(src + (c0 + e) * BM + r);
+            for (int e = 0; e < 32; ++e) a[e] += __ldcg(src + (c0 + e) * BM + r);
           }
-          if (!row_ok) continue;
-          const int col0 = tn * BN + c0;
+          __syncwarp();  // the previous block's reads of the staging are done
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int col = col0 + q * 4;
-            float o[4];
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(stage + lane * EPI_PITCH + q * 4) =
+                make_float4(a[q * 4], a[q * 4 + 1], a[q * 4 + 2], a[q * 4 + 3]);
+          __syncwarp();
+          const int col = tn * BN + c0 + sub_c;
+          const int row0 = tm * BM + quarter * 32 + sub_r;  // + 4 g for access g
+          const bool full = vec && col + 3 < p.N;
+          // every read of C is issued before any write, so the reads overlap
+          float4 old[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[e] = p.alpha * a[q * 4 + e];
-            if (vec && col + 3 < p.N) {
-              float4 w4 = make_float4(o[0], o[1], o[2], o[3]);
-              if (p.beta != 0.f) {
-                const float4 c = *reinterpret_cast<const float4*>(crow + col);
-                w4.x = fmaf(p.beta, c.x, o[0]);
-                w4.y = fmaf(p.beta, c.y, o[1]);
-                w4.z = fmaf(p.beta, c.z, o[2]);
-                w4.w = fmaf(p.beta, c.w, o[3]);
-              }
-              *reinterpret_cast<float4*>(crow + col) = w4;
+          for (int g = 0; g < 8; ++g) {
+            old[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int row = row0 + 4 * g;
+            if (p.beta == 0.f || row >= p.M) continue;
+            const float* cp = p.C + (long long)row * p.ldc + col;
+            if (full) {
+              old[g] = *reinterpret_cast<const float4*>(cp);
             } else {
+              if (col + 0 < p.N) old[g].x = cp[0];
+              if (col + 1 < p.N) old[g].y = cp[1];
+              if (col + 2 < p.N) old[g].z = cp[2];
+              if (col + 3 < p.N) old[g].w = cp[3];
+            }
+          }
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (col + e < p.N)
-                  crow[col + e] = p.beta != 0.f ? fmaf(p.beta, crow[col + e], o[e]) : o[e];
+          for (int g = 0; g < 8; ++g) {
+            const int row = row0 + 4 * g;
+            if (row >= p.M) continue;
+            const float4 t =
+                *reinterpret_cast<const float4*>(stage + (sub_r + 4 * g) * EPI_PITCH + sub_c);
+            float4 w4 = make_float4(p.alpha * t.x, p.alpha * t.y, p.alpha * t.z, p.alpha * t.w);
+            if (p.beta != 0.f) {
+              w4.x = fmaf(p.beta, old[g].x, w4.x);
+              w4.y = fmaf(p.beta, old[g].y, w4.y);
+              w4.z = fmaf(p.beta, old[g].z, w4.z);
+              w4.w = fmaf(p.beta, old[g].w, w4.w);
+            }
+            float* cp = p.C + (long long)row * p.ldc + col;
+            if (full) {
+              *reinterpret_cast<float4*>(cp) = w4;
+            } else {
+              if (col + 0 < p.N) cp[0] = w4.x;
+              if (col + 1 < p.N) cp[1] = w4.y;
+              if (col + 2 < p.N) cp[2] = w4.z;
+              if (col + 3 < p.N) cp[3] = w4.w;
             }
           }
         }
@@ -477,13 +535,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 bool encode_k_major(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const float* base,
-                    int rows, int K, long long ldw, int box_rows) {
+                    int rows, int K, long long ldw, int box_rows, int bk) {
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ldw * 4};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -527,10 +586,11 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     std::lock_guard<std::mutex> lock(x3::g_mutex);
     if (dev < 0 || dev >= 64) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     if (!x3::g_ready[dev]) {
-      if (cudaFuncSetAttribute(x3::gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               x3::SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(x3::gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               x3::SMEM_BYTES) != cudaSuccess) {
+      const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+      if (cudaFuncSetAttribute(x3::gemm_kernel<1, 16>, attr, x3::SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(x3::gemm_kernel<2, 16>, attr, x3::SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(x3::gemm_kernel<1, 32>, attr, x3::SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(x3::gemm_kernel<2, 32>, attr, x3::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
       }
@@ -547,12 +607,14 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
       qc.dynamicSmemBytes = x3::SMEM_BYTES;
       qc.attrs = qa;
       qc.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, x3::gemm_kernel<2>, &qc) != cudaSuccess) {
+      // both widths have the same block and shared-memory size; take the smaller
+      int n16 = 0, n32 = 0;
+      if (cudaOccupancyMaxActiveClusters(&n16, x3::gemm_kernel<2, 16>, &qc) != cudaSuccess ||
+          cudaOccupancyMaxActiveClusters(&n32, x3::gemm_kernel<2, 32>, &qc) != cudaSuccess) {
         cudaGetLastError();
-        n = 0;
+        n16 = n32 = 0;
       }
-      x3::g_pairs[dev] = n;
+      x3::g_pairs[dev] = n16 < n32 ? n16 : n32;
       x3::g_ready[dev] = true;
     }
     pairs = x3::g_pairs[dev];
@@ -569,14 +631,16 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   // the pair form a schedule unit is two vertically adjacent tiles (a tile row
   // pair), handed to one cluster.
   const int tiles_m = (M + x3::BM - 1) / x3::BM, tiles_n = (N + x3::BN - 1) / x3::BN;
-  const int kiters = (K + x3::BK - 1) / x3::BK;
-  Schedule sched = make_schedule((tiles_m + 1) / 2, tiles_n, kiters, pairs, 4, 2);
+  const int bk = K >= 1024 ? 16 : 32;  // the k-slice width (see Slice)
+  const int kiters = (K + bk - 1) / bk;
+  const int min_units = 64 / bk;  // at least 64 of K per CTA in a split
+  Schedule sched = make_schedule((tiles_m + 1) / 2, tiles_n, kiters, pairs, 4, min_units);
   if (CL == 2 && sched.dp_tiles == 0) {
     // every tile is split along K: the pairs' lockstep costs more than the
     // shared B tiles save (measured at 1024^3, 2048^3 and 16384 x 64 x 4096)
     CL = 1;
   }
-  if (CL == 1) sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, 2);
+  if (CL == 1) sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, min_units);
   const bool split = sched.dp_tiles < sched.tiles;
   const int ctas = sched.grid * CL;
 
@@ -612,10 +676,10 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
 
   // 2. tensor-core GEMM
   CUtensorMap mA_hi, mA_lo, mB_hi, mB_lo;
-  if (!x3::encode_k_major(enc, &mA_hi, a_hi, M, K, Kp, x3::BM) ||
-      !x3::encode_k_major(enc, &mA_lo, a_lo, M, K, Kp, x3::BM) ||
-      !x3::encode_k_major(enc, &mB_hi, b_hi, N, K, Kp, x3::BN / CL) ||
-      !x3::encode_k_major(enc, &mB_lo, b_lo, N, K, Kp, x3::BN / CL))
+  if (!x3::encode_k_major(enc, &mA_hi, a_hi, M, K, Kp, x3::BM, bk) ||
+      !x3::encode_k_major(enc, &mA_lo, a_lo, M, K, Kp, x3::BM, bk) ||
+      !x3::encode_k_major(enc, &mB_hi, b_hi, N, K, Kp, x3::BN / CL, bk) ||
+      !x3::encode_k_major(enc, &mB_lo, b_lo, N, K, Kp, x3::BN / CL, bk))
     return SGEMM_ERR_LAUNCH;
   x3::Params p;
   p.M = M;
@@ -632,7 +696,12 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   p.status = status;
   p.timeout_ns = library_wait_timeout_ns();
   if (CL == 1) {
-    x3::gemm_kernel<1><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi, mB_lo);
+    if (bk == 16)
+      x3::gemm_kernel<1, 16><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi,
+                                                                        mB_lo);
+    else
+      x3::gemm_kernel<1, 32><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi,
+                                                                        mB_lo);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
   } else {
     cudaLaunchConfig_t lc = {};
@@ -647,8 +716,10 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     lc.stream = stream;
     lc.attrs = la;
     lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, x3::gemm_kernel<2>, p, mA_hi, mA_lo, mB_hi, mB_lo) !=
-        cudaSuccess) {
+    const cudaError_t e =
+        bk == 16 ? cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 16>, p, mA_hi, mA_lo, mB_hi, mB_lo)
+                 : cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 32>, p, mA_hi, mA_lo, mB_hi, mB_lo);
+    if (e != cudaSuccess) {
       cudaGetLastError();
       return SGEMM_ERR_LAUNCH;
     }
@@ -656,7 +727,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   char text[160];
   snprintf(text, sizeof(text),
            "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d grid=%d units=%d dp=%d split=%d kiters=%d",
-           x3::BM, x3::BN, x3::BK, x3::ST, CL, ctas, sched.grid, sched.dp_tiles,
+           x3::BM, x3::BN, bk, 64 / bk, CL, ctas, sched.grid, sched.dp_tiles,
            sched.tiles - sched.dp_tiles, kiters);
   note_last_config(text);
   return SGEMM_OK;

@@ -91,3 +91,11 @@ def test_named_integer_bit_exact(name):
 @pytest.mark.parametrize("n", [s for s in SWEEP_SIZES if s <= 8192])
 def test_sweep_integer_bit_exact(n):
     H.check_sampled(WORKLOADS[f"sweep{n}_int"], rows=4, elements=512, fn=X3)
+
+
+def test_slice_width_follows_k():
+    # BK = 32 (two stages) below K = 1024, BK = 16 (four stages) from there
+    H.check_against_oracle(Workload("x3k", 200, 300, 1023, 1.0, 0.5, "int3", 38), fn=X3)
+    assert "128x256x32_s2" in binding.sgemm_last_config()
+    H.check_against_oracle(Workload("x3k", 200, 300, 1024, 1.0, 0.5, "int3", 38), fn=X3)
+    assert "128x256x16_s4" in binding.sgemm_last_config()
