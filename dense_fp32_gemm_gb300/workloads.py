@@ -125,3 +125,63 @@ def element_sample(M: int, N: int, count: int, seed: int):
     r = torch.randint(0, M, (count,), generator=gen)
     c = torch.randint(0, N, (count,), generator=gen)
     return r.tolist(), c.tolist()
+
+
+# ---- counter-based integer matrices for the largest sizes ----------------------
+# A matrix of more than 2^31 elements is too large to draw on the host in one
+# piece for every test run, and a sequential generator cannot produce a chosen
+# row or column on its own. These matrices are instead a pure function of
+# (seed, row, column): element (i, j) of a rows x cols matrix is
+#     h = fmix32((idx mod 2^32) xor fmix32((idx div 2^32) xor seed)),  idx = i*cols + j
+#     value = (h mod 7) - 3        (an integer in {-3..3})
+# where fmix32 is the 32-bit finalizer of MurmurHash3 (Austin Appleby). The
+# same torch integer arithmetic runs on the device (the whole matrix, in row
+# blocks) and on the host (only the rows or columns a check needs).
+
+_M32 = 0xFFFFFFFF
+
+
+def fmix32(h: torch.Tensor) -> torch.Tensor:
+    """MurmurHash3's 32-bit finalizer on int64 tensors holding values below
+    2^32 (products wrap modulo 2^64; only their low 32 bits are kept)."""
+    h = h ^ (h >> 16)
+    h = (h * 0x85EBCA6B) & _M32
+    h = h ^ (h >> 13)
+    h = (h * 0xC2B2AE35) & _M32
+    return h ^ (h >> 16)
+
+
+def hashed_int3(seed: int, idx: torch.Tensor) -> torch.Tensor:
+    """Values in {-3..3} (float32) of the elements with linear indices `idx`
+    (int64, row-major) of a counter-based matrix with this seed."""
+    hi = fmix32(((idx >> 32) ^ seed) & _M32)
+    h = fmix32((idx & _M32) ^ hi)
+    return ((h % 7) - 3).to(torch.float32)
+
+
+def hashed_int3_rows(seed: int, cols: int, rows, device="cpu") -> torch.Tensor:
+    """The listed rows (a list or a range) of a counter-based rows x cols
+    matrix, as a len(rows) x cols float32 tensor on `device`."""
+    r = torch.as_tensor(list(rows), dtype=torch.int64, device=device)
+    j = torch.arange(cols, dtype=torch.int64, device=device)
+    return hashed_int3(seed, r[:, None] * cols + j[None, :])
+
+
+def hashed_int3_cols(seed: int, rows: int, cols: int, col_list, device="cpu") -> torch.Tensor:
+    """The listed columns of a counter-based rows x cols matrix, as a
+    rows x len(col_list) float32 tensor."""
+    i = torch.arange(rows, dtype=torch.int64, device=device)
+    c = torch.as_tensor(list(col_list), dtype=torch.int64, device=device)
+    return hashed_int3(seed, i[:, None] * cols + c[None, :])
+
+
+def hashed_int3_device(seed: int, rows: int, cols: int, device="cuda",
+                       block_elems: int = 1 << 27) -> torch.Tensor:
+    """The whole rows x cols counter-based matrix on `device` (dense,
+    row-major), filled in blocks of rows."""
+    out = torch.empty((rows, cols), dtype=torch.float32, device=device)
+    step = max(1, block_elems // max(cols, 1))
+    for r0 in range(0, rows, step):
+        out[r0: r0 + step] = hashed_int3_rows(seed, cols, range(r0, min(rows, r0 + step)),
+                                              device=device)
+    return out
