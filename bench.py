@@ -234,9 +234,28 @@ def cpu_baseline(w, A, B, C, budget_s=10.0):
             break
         rows = min(w.M, max(rows * 2, int(rows * (budget_s / 4) / max(dt, 1e-3))))
     value = gemm_flops(total_rows, w.N, w.K) / spent / 1e9
+    # one core, on a few rows (about a second)
+    one_rows = max(1, min(w.M, int(total_rows * 0.2 / max(threads, 1))))
+    one_dt = oracle_rows_timing(w, A, B, C, one_rows, 1)
     return {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "single_core_value": round(gemm_flops(one_rows, w.N, w.K) / one_dt / 1e9, 3),
+            "cpu_model": cpu_model(),
             "sample": f"first {total_rows} of {w.M} rows of C ({w.N} columns, K={w.K}), "
-                      f"{spent:.2f} s, FP64 i-j-k loop, rows split over {threads} threads"}
+                      f"{spent:.2f} s, FP64 i-j-k loop, rows split over {threads} threads; "
+                      f"single core: first {one_rows} rows, {one_dt:.2f} s"}
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu), or the platform's processor string."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 # ---- arms ---------------------------------------------------------------------------
