@@ -580,6 +580,39 @@ def run_report(args):
         torch.cuda.empty_cache()
 
 
+# Oracle timing per workload: whole problems up to 4096^3; at 8192^3 and
+# 16384^3 a 256-row sample, extrapolated to the whole problem.
+ORACLE_REPORT = ["square128", "square4096", "edges8191x1000x777", "kdominant1024x1024x16384",
+                 "skinny16384x64x4096"] + [f"sweep{n}" for n in (256, 512, 1024, 2048, 8192, 16384)]
+ORACLE_SAMPLE_ROWS = 256
+
+
+def run_oracle_report(args):
+    """The CPU oracle timed on the host cores (all of them, and one), one JSON
+    line per workload. Runs on the host only."""
+    from dense_fp32_gemm_gb300.workloads import WORKLOADS, make_inputs
+    threads = len(os.sched_getaffinity(0))
+    model = cpu_model()
+    for name in ORACLE_REPORT:
+        w = WORKLOADS[name]
+        A, B, C = make_inputs(w)
+        rows = w.M if w.M * w.N * w.K <= 4096 ** 3 else min(w.M, ORACLE_SAMPLE_ROWS)
+        t_all = oracle_rows_timing(w, A, B, C, rows, threads)
+        per_row_one_core = t_all * threads / rows
+        rows1 = max(1, min(rows, int(1.0 / max(per_row_one_core, 1e-9))))
+        t_one = oracle_rows_timing(w, A, B, C, rows1, 1)
+        print(json.dumps({
+            "workload": name, "M": w.M, "N": w.N, "K": w.K, "rows_timed": rows,
+            "extrapolated": rows < w.M,
+            "all_cores": threads, "all_core_gflops": round(gemm_flops(rows, w.N, w.K) / t_all / 1e9, 3),
+            "all_core_s_whole_problem": round(t_all * w.M / rows, 3),
+            "single_core_rows": rows1,
+            "single_core_gflops": round(gemm_flops(rows1, w.N, w.K) / t_one / 1e9, 3),
+            "single_core_s_whole_problem": round(t_one * w.M / rows1, 3),
+            "cpu_model": model}), flush=True)
+        del A, B, C
+
+
 def run_ladder(args):
     """The pages' kernels 3, 7 and 8 next to the library's own kernel on one
     workload (default: the 4096 cube), one JSON line each."""
@@ -648,6 +681,8 @@ def main(argv=None):
                     help="time every named workload and the sweep, one JSON line each")
     ap.add_argument("--ladder", action="store_true",
                     help="time the pages' kernels 3, 7, 8 and sgemm on --workload")
+    ap.add_argument("--oracle-report", action="store_true",
+                    help="time the CPU oracle on every workload (host only)")
     ap.add_argument("--profile-once", action="store_true",
                     help="with --ladder: warm-up calls plus one call per kernel, no timing")
     args = ap.parse_args(argv)
@@ -658,6 +693,9 @@ def main(argv=None):
         return
     if args.ladder:
         run_ladder(args)
+        return
+    if args.oracle_report:
+        run_oracle_report(args)
         return
     from dense_fp32_gemm_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
