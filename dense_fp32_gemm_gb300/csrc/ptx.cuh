@@ -100,6 +100,13 @@ __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtens
       : "memory");
 }
 
+// Orders this thread's earlier generic-proxy writes to shared memory before
+// later async-proxy reads of it (TMA stores, tensor-core operand reads) that
+// are ordered after this point through a barrier.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Rank of this CTA in its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

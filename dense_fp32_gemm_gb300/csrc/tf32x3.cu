@@ -12,16 +12,22 @@
 // product on the TF32 tensor cores with FP32 accumulation. Integer inputs up
 // to 2^11 in magnitude are exact TF32 values (x_lo = 0), so they stay exact.
 //
+// x_hi is never stored: the TF32 MMA reads an FP32 value's sign, exponent and
+// top 10 mantissa bits and ignores the low 13, which is exactly x_hi. (Measured
+// on GB300: results with x_hi = x and with x_hi = trunc(x) are bit-identical;
+// the parity tests hold the path to the oracle either way.)
+//
 // Data flow:
-//   1. split kernels write A_hi, A_lo (M x K, K-major) and the transposed
-//      B_hi, B_lo (N x K, K-major) into the per-stream workspace, with rows
-//      padded to a multiple of 4 floats for TMA;
-//   2. the GEMM kernel (one CTA of 6 warps per SM, persistent over 128 x 256
-//      tiles): warp 0 issues TMA loads of the four operand tiles of each
-//      32-wide k-slice (128-byte swizzle) into a 2-stage ring; warp 1 owns a
-//      256-column TMEM accumulator and issues, per 8-wide k-step, the three
-//      tcgen05.mma.kind::tf32 products; warps 2-5 read the accumulator back
-//      with tcgen05.ld and apply alpha * acc + beta * C.
+//   1. B is transposed into the per-stream workspace (N x K, K-major, rows
+//      padded to a multiple of 4 floats for TMA); A is read where it is when
+//      its rows are 16-byte aligned, else copied there too;
+//   2. the GEMM kernel (one CTA of 10 warps per SM, persistent over 128 x 256
+//      tiles): warp 0 issues TMA loads of the raw A and B^T tiles of each
+//      k-slice (swizzled) into a ring of stages; warps 6-9 write the
+//      residual tiles A_lo, B_lo beside them in the same stage; warp 1 owns
+//      two 256-column TMEM accumulators and issues, per 8-wide k-step, the
+//      three tcgen05.mma.kind::tf32 products; warps 2-5 read an accumulator
+//      back with tcgen05.ld and apply alpha * acc + beta * C.
 //
 // Cluster form (CL = 2, the default where the device can co-schedule CTA
 // pairs): the two CTAs of a cluster compute vertically adjacent tiles (tile
@@ -64,7 +70,7 @@ long long library_wait_timeout_ns();
 
 namespace x3 {
 
-constexpr int BM = 128, BN = 256, NT = 192;
+constexpr int BM = 128, BN = 256, NT = 320;
 
 // The k-slice: BK values of K per stage, in swizzled rows of 4 * BK bytes,
 // with as many stages as fit in 192 KB. BK = 16 (four 48 KB stages, 64-byte
@@ -80,6 +86,8 @@ struct Slice {
   static constexpr int ST = 64 / BK;
   static constexpr int A_BYTES = BM * BK * 4;                      // one of A_hi, A_lo
   static constexpr int B_BYTES = BN * BK * 4;                      // one of B_hi, B_lo
+  // a stage: [A_hi | A_lo | B_hi | B_lo]; TMA writes the _hi tiles (the raw
+  // values), the converter warps the _lo tiles
   static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 or 48 KB
 };
 constexpr int kMaxStages = 4;
@@ -90,11 +98,14 @@ static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
 constexpr int ACC_COLS = BN;              // one FP32 accumulator: 128 lanes x BN columns
 constexpr int TMEM_COLS = 2 * ACC_COLS;   // two, so the epilogue overlaps the next MMAs
 constexpr int EPI_THREADS = 128;          // warps 2-5
+constexpr int CONV_WARP0 = 6;             // warps 6-9 write the residual tiles
+constexpr int CONV_THREADS = 128;
 constexpr uint32_t IDESC = tc::idesc_tf32(BM, BN);
 static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
 
 struct Barriers {
-  uint64_t full[kMaxStages];   // TMA transaction bytes of one stage
+  uint64_t full[kMaxStages];   // TMA transaction bytes of one stage (the raw tiles)
+  uint64_t conv[kMaxStages];   // the converter warps have written the stage's residuals
   uint64_t empty[kMaxStages];  // MMAs that read a stage have completed
   uint64_t tmem_full[2];   // a piece's last MMA into accumulator i has completed
   uint64_t tmem_empty[2];  // the epilogue warps have read accumulator i
@@ -129,43 +140,23 @@ __device__ __forceinline__ float tf32_trunc(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
-// A (M x K, lda) -> A_hi, A_lo (M x K, ldw). Rows over blockIdx.y (strided
-// by gridDim.y), groups of 4 columns over x; 128-bit loads and stores when
-// the row starts of A are 16-byte aligned (ldw is a multiple of 4).
-__global__ void split_a_kernel(int M, int K, const float* __restrict__ A, long long lda,
-                               float* __restrict__ hi, float* __restrict__ lo, long long ldw,
-                               int vec) {
-  const int groups = (K + 3) / 4;
+// A (M x K, lda) -> a copy with rows of ldw floats (a multiple of 4), for an A
+// whose rows are not 16-byte aligned (TMA needs them to be). Rows over
+// blockIdx.y (strided by gridDim.y), columns over x.
+__global__ void pack_a_kernel(int M, int K, const float* __restrict__ A, long long lda,
+                              float* __restrict__ out, long long ldw) {
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
     const float* a = A + (long long)m * lda;
-    float* h = hi + (long long)m * ldw;
-    float* l = lo + (long long)m * ldw;
-    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += gridDim.x * blockDim.x) {
-      const int k = g * 4;
-      if (vec && k + 3 < K) {
-        const float4 x = *reinterpret_cast<const float4*>(a + k);
-        const float4 xh = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z),
-                                      tf32_trunc(x.w));
-        *reinterpret_cast<float4*>(h + k) = xh;
-        *reinterpret_cast<float4*>(l + k) =
-            make_float4(tf32_trunc(x.x - xh.x), tf32_trunc(x.y - xh.y), tf32_trunc(x.z - xh.z),
-                        tf32_trunc(x.w - xh.w));
-      } else {
-        for (int e = 0; e < 4 && k + e < K; ++e) {
-          const float x = a[k + e];
-          const float xh = tf32_trunc(x);
-          h[k + e] = xh;
-          l[k + e] = tf32_trunc(x - xh);
-        }
-      }
-    }
+    float* o = out + (long long)m * ldw;
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x)
+      o[k] = a[k];
   }
 }
 
-// B (K x N, ldb) -> transposed B_hi, B_lo (N x K, ldw), through 32 x 32
-// shared-memory tiles so that both the reads and the writes are coalesced.
-__global__ void split_bt_kernel(int K, int N, const float* __restrict__ B, long long ldb,
-                                float* __restrict__ hi, float* __restrict__ lo, long long ldw) {
+// B (K x N, ldb) -> B^T (N x K, ldw), through 32 x 32 shared-memory tiles so
+// that both the reads and the writes are coalesced.
+__global__ void transpose_b_kernel(int K, int N, const float* __restrict__ B, long long ldb,
+                                   float* __restrict__ bt, long long ldw) {
   __shared__ float tile[32][33];
   const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
@@ -176,13 +167,14 @@ __global__ void split_bt_kernel(int K, int N, const float* __restrict__ B, long 
   __syncthreads();
   for (int j = 0; j < 32; j += 8) {
     const int n = n0 + ty + j, k = k0 + tx;
-    if (n < N && k < K) {
-      const float x = tile[tx][ty + j];
-      const float h = tf32_trunc(x);
-      hi[(long long)n * ldw + k] = h;
-      lo[(long long)n * ldw + k] = tf32_trunc(x - h);
-    }
+    if (n < N && k < K) bt[(long long)n * ldw + k] = tile[tx][ty + j];
   }
+}
+
+// The residual x_lo of four raw values.
+__device__ __forceinline__ float4 tf32_residual4(float4 x) {
+  return make_float4(tf32_trunc(x.x - tf32_trunc(x.x)), tf32_trunc(x.y - tf32_trunc(x.y)),
+                     tf32_trunc(x.z - tf32_trunc(x.z)), tf32_trunc(x.w - tf32_trunc(x.w)));
 }
 
 __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {
@@ -197,9 +189,8 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc
 
 template <int CL, int BK>
 __global__ void __launch_bounds__(NT, 1)
-    gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmA_hi,
-                const __grid_constant__ CUtensorMap tmA_lo, const __grid_constant__ CUtensorMap tmB_hi,
-                const __grid_constant__ CUtensorMap tmB_lo) {
+    gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmA,
+                const __grid_constant__ CUtensorMap tmB) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -224,6 +215,7 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bar->full[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&bar->conv[s]), CONV_THREADS / 32);
       ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), CL);
     }
     for (int i = 0; i < 2; ++i) {
@@ -234,10 +226,8 @@ __global__ void __launch_bounds__(NT, 1)
     ptx::mbar_init(ptx::smem_addr(&bar->epi_sync), EPI_THREADS);
     bar->abort = 0;
     ptx::mbar_fence_init();
-    ptx::tma_prefetch_desc(&tmA_hi);
-    ptx::tma_prefetch_desc(&tmA_lo);
-    ptx::tma_prefetch_desc(&tmB_hi);
-    ptx::tma_prefetch_desc(&tmB_lo);
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
     tc::tmem_alloc(ptx::smem_addr(&bar->tmem_addr), TMEM_COLS);
@@ -251,7 +241,7 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tmem = bar->tmem_addr;
 
   if (warp == 0) {
-    // ---- TMA producer: the four operand tiles of every k-slice of every piece
+    // ---- TMA producer: the raw A and B^T tiles of every k-slice of every piece
     if (lane == 0) {
       int it = 0;
       for (int i = 0; i < npieces && !*abort_w; ++i) {
@@ -270,19 +260,15 @@ __global__ void __launch_bounds__(NT, 1)
           }
           const uint32_t fb = ptx::smem_addr(&bar->full[s]);
           const uint32_t st0 = base_addr + (uint32_t)(s * STAGE_BYTES);
-          ptx::mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
-          ptx::tma_load_2d(st0, &tmA_hi, kb * BK, tm * BM, fb);
-          ptx::tma_load_2d(st0 + A_BYTES, &tmA_lo, kb * BK, tm * BM, fb);
+          ptx::mbar_arrive_expect_tx(fb, (uint32_t)(A_BYTES + B_BYTES));
+          ptx::tma_load_2d(st0, &tmA, kb * BK, tm * BM, fb);
           if (CL == 1) {
-            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB_hi, kb * BK, tn * BN, fb);
-            ptx::tma_load_2d(st0 + 2 * A_BYTES + B_BYTES, &tmB_lo, kb * BK, tn * BN, fb);
+            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN, fb);
           } else {
-            // this CTA's half of each B tile, into both CTAs
+            // this CTA's half of the B tile, into both CTAs
             const uint32_t half = (uint32_t)(rank * (B_BYTES / 2));
             const int row = tn * BN + rank * (BN / 2);
-            ptx::tma_load_2d_multicast(st0 + 2 * A_BYTES + half, &tmB_hi, kb * BK, row, fb, kPair);
-            ptx::tma_load_2d_multicast(st0 + 2 * A_BYTES + B_BYTES + half, &tmB_lo, kb * BK, row,
-                                       fb, kPair);
+            ptx::tma_load_2d_multicast(st0 + 2 * A_BYTES + half, &tmB, kb * BK, row, fb, kPair);
           }
         }
         if (!ok) break;
@@ -322,7 +308,10 @@ __global__ void __launch_bounds__(NT, 1)
         bool ok = true;
         for (int kb = pc.kb; kb < pc.ke; ++kb, ++it) {
           const int s = it % ST;
+          // the raw tiles (TMA) and the residual tiles (converter warps)
           if (!bounded_wait(ptx::smem_addr(&bar->full[s]), (uint32_t)((it / ST) & 1), abort_w,
+                            p.status, kDevTimeoutFull, p.timeout_ns) ||
+              !bounded_wait(ptx::smem_addr(&bar->conv[s]), (uint32_t)((it / ST) & 1), abort_w,
                             p.status, kDevTimeoutFull, p.timeout_ns)) {
             ok = false;
             break;
@@ -358,6 +347,38 @@ __global__ void __launch_bounds__(NT, 1)
         const uint64_t t0 = ptx::global_ns();
         while (!ptx::mbar_try_wait(ptx::smem_addr(&bar->drain), 0u))
           if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+      }
+    }
+  } else if (warp >= CONV_WARP0) {
+    // ---- converter warps 6-9: x_lo = trunc(x - trunc(x)) of every raw value of
+    // a stage, written at the same offset in the stage's _lo tile (the tiles
+    // have one shape and swizzle, so a value keeps its position) -------------
+    const int ct = tid - CONV_WARP0 * 32;
+    int it = 0;
+    bool ok = true;
+    for (int i = 0; i < npieces && ok && !*abort_w; ++i) {
+      const Piece pc = get_piece(sc, b, i);
+      for (int kb = pc.kb; kb < pc.ke; ++kb, ++it) {
+        const int s = it % ST;
+        ok = bounded_wait(ptx::smem_addr(&bar->full[s]), (uint32_t)((it / ST) & 1), abort_w,
+                          p.status, kDevTimeoutFull, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        unsigned char* st = base + s * STAGE_BYTES;
+        const float4* a_raw = reinterpret_cast<const float4*>(st);
+        float4* a_lo = reinterpret_cast<float4*>(st + A_BYTES);
+        const float4* b_raw = reinterpret_cast<const float4*>(st + 2 * A_BYTES);
+        float4* b_lo = reinterpret_cast<float4*>(st + 2 * A_BYTES + B_BYTES);
+#pragma unroll
+        for (int q = ct; q < A_BYTES / 16; q += CONV_THREADS) a_lo[q] = tf32_residual4(a_raw[q]);
+#pragma unroll
+        for (int q = ct; q < B_BYTES / 16; q += CONV_THREADS) b_lo[q] = tf32_residual4(b_raw[q]);
+        // the MMAs read these tiles through the async proxy
+        ptx::fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bar->conv[s]));
       }
     }
   } else {
@@ -644,42 +665,41 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   const bool split = sched.dp_tiles < sched.tiles;
   const int ctas = sched.grid * CL;
 
-  // workspace: A_hi, A_lo (M x Kp), B_hi, B_lo transposed (N x Kp), then one
-  // partial tile per CTA when the schedule splits
+  // workspace: B^T (N x Kp), a copy of A (M x Kp) only when A's rows are not
+  // 16-byte aligned, then one partial tile per CTA when the schedule splits
   const long long Kp = ((long long)K + 3) / 4 * 4;
-  const size_t split_floats = (size_t)(2 * (long long)M * Kp + 2 * (long long)N * Kp);
+  const bool a_direct = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0);
+  const size_t bt_floats = (size_t)N * Kp;
+  const size_t a_floats = a_direct ? 0 : (size_t)M * Kp;
   const size_t partial_floats = split ? (size_t)ctas * x3::BM * x3::BN : 0;
   float* ws = nullptr;
   int* status = nullptr;
   uint32_t* flags = nullptr;
   uint32_t epoch = 0;
-  st = library_workspace(dev, stream, split_floats + partial_floats, (size_t)ctas, &ws, &status,
-                         &flags, &epoch);
+  st = library_workspace(dev, stream, bt_floats + a_floats + partial_floats, (size_t)ctas, &ws,
+                         &status, &flags, &epoch);
   if (st != SGEMM_OK) return st;
-  float* a_hi = ws;
-  float* a_lo = a_hi + (size_t)M * Kp;
-  float* b_hi = a_lo + (size_t)M * Kp;
-  float* b_lo = b_hi + (size_t)N * Kp;
-  float* partials = b_lo + (size_t)N * Kp;
+  float* bt = ws;
+  float* a_copy = bt + bt_floats;
+  float* partials = a_copy + a_floats;
 
-  // 1. split (and transpose B)
+  // 1. B^T (and, when needed, an aligned copy of A)
   {
-    const int groups = (K + 3) / 4;
-    const int bx = (groups + 127) / 128 < 8 ? (groups + 127) / 128 : 8;
-    const int by = M < 65535 ? M : 65535;
-    const int vec = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0);
-    x3::split_a_kernel<<<dim3(bx, by), 128, 0, stream>>>(M, K, A, lda, a_hi, a_lo, Kp, vec);
     dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
-    x3::split_bt_kernel<<<grid, block, 0, stream>>>(K, N, B, ldb, b_hi, b_lo, Kp);
+    x3::transpose_b_kernel<<<grid, block, 0, stream>>>(K, N, B, ldb, bt, Kp);
+    if (!a_direct) {
+      const int bx = (K + 255) / 256 < 8 ? (K + 255) / 256 : 8;
+      const int by = M < 65535 ? M : 65535;
+      x3::pack_a_kernel<<<dim3(bx, by), 256, 0, stream>>>(M, K, A, lda, a_copy, Kp);
+    }
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
   }
 
-  // 2. tensor-core GEMM
-  CUtensorMap mA_hi, mA_lo, mB_hi, mB_lo;
-  if (!x3::encode_k_major(enc, &mA_hi, a_hi, M, K, Kp, x3::BM, bk) ||
-      !x3::encode_k_major(enc, &mA_lo, a_lo, M, K, Kp, x3::BM, bk) ||
-      !x3::encode_k_major(enc, &mB_hi, b_hi, N, K, Kp, x3::BN / CL, bk) ||
-      !x3::encode_k_major(enc, &mB_lo, b_lo, N, K, Kp, x3::BN / CL, bk))
+  // 2. tensor-core GEMM on the raw tiles
+  CUtensorMap mA, mB;
+  if (!x3::encode_k_major(enc, &mA, a_direct ? A : a_copy, M, K, a_direct ? (long long)lda : Kp,
+                          x3::BM, bk) ||
+      !x3::encode_k_major(enc, &mB, bt, N, K, Kp, x3::BN / CL, bk))
     return SGEMM_ERR_LAUNCH;
   x3::Params p;
   p.M = M;
@@ -697,11 +717,9 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   p.timeout_ns = library_wait_timeout_ns();
   if (CL == 1) {
     if (bk == 16)
-      x3::gemm_kernel<1, 16><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi,
-                                                                        mB_lo);
+      x3::gemm_kernel<1, 16><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
     else
-      x3::gemm_kernel<1, 32><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA_hi, mA_lo, mB_hi,
-                                                                        mB_lo);
+      x3::gemm_kernel<1, 32><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
   } else {
     cudaLaunchConfig_t lc = {};
@@ -717,8 +735,8 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     lc.attrs = la;
     lc.numAttrs = 1;
     const cudaError_t e =
-        bk == 16 ? cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 16>, p, mA_hi, mA_lo, mB_hi, mB_lo)
-                 : cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 32>, p, mA_hi, mA_lo, mB_hi, mB_lo);
+        bk == 16 ? cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 16>, p, mA, mB)
+                 : cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 32>, p, mA, mB);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return SGEMM_ERR_LAUNCH;
@@ -726,9 +744,9 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   }
   char text[160];
   snprintf(text, sizeof(text),
-           "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d grid=%d units=%d dp=%d split=%d kiters=%d",
+           "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d grid=%d units=%d dp=%d split=%d kiters=%d%s",
            x3::BM, x3::BN, bk, 64 / bk, CL, ctas, sched.grid, sched.dp_tiles,
-           sched.tiles - sched.dp_tiles, kiters);
+           sched.tiles - sched.dp_tiles, kiters, a_direct ? "" : " a=copied");
   note_last_config(text);
   return SGEMM_OK;
 }

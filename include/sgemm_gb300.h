@@ -91,8 +91,9 @@ int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float
  * high part and a TF32 residual; the dropped residual product is below
  * 3 * 2^-20 of sum |a||b|, inside the library's FP32 tolerance, and integer
  * inputs up to 2^11 stay exact). The pages have no tensor-core kernel; this is
- * the split-operand method of Ootomo and Yokota (2022). It uses 8 * (M + N) *
- * K bytes of workspace for the split operands. Reported separately from the
+ * the split-operand method of Ootomo and Yokota (2022). It uses 4 * N * K
+ * bytes of workspace for a transposed copy of B, plus 4 * M * K when the rows
+ * of A are not 16-byte aligned (A is then copied). Reported separately from the
  * FFMA path.
  */
 int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
