@@ -387,7 +387,7 @@ def run_ours(args, w):
         tf32x3 = {"value": round(v3, 1), "unit": UNIT, "ms_per_step": round(t3 / args.steps * 1e3, 4),
                   "config": binding.sgemm_last_config(),
                   "note": "opt-in sgemm_3xtf32: split-operand TF32 on tcgen05, same FP32 tolerance; "
-                          "includes its split pre-pass kernels"}
+                          "includes its B-transpose pre-pass kernel"}
 
     # ---- end to end from pinned host buffers, through the C ABI ---------------------
     # sgemm_host copies A, B (and C, as beta != 0) from pinned host memory,
