@@ -1,0 +1,7 @@
+// cfg_small_f2_ku16.cu -- instantiation of the FFMA kernel for CfgSmallF2Ku16 (one translation
+// unit per configuration so that the library compiles in parallel).
+#include "launch.cuh"
+
+namespace sgemm_gb300 {
+SGEMM_GB300_DEFINE_ENTRY(CfgSmallF2Ku16, kEntrySmallF2Ku16)
+}  // namespace sgemm_gb300

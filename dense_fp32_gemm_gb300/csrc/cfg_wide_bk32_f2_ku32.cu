@@ -1,0 +1,7 @@
+// cfg_wide_bk32_f2_ku32.cu -- instantiation of the FFMA kernel for CfgWideBk32F2Ku32 (one translation
+// unit per configuration so that the library compiles in parallel).
+#include "launch.cuh"
+
+namespace sgemm_gb300 {
+SGEMM_GB300_DEFINE_ENTRY(CfgWideBk32F2Ku32, kEntryWideBk32F2Ku32)
+}  // namespace sgemm_gb300
