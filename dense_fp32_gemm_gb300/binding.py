@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_ladder": (I, [I, I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_3xtf32_set_cluster_size": (I, [I]),
                 "sgemm_host_set_pipeline": (I, [I, I, I, I]),
+                "sgemm_config_layouts": (I, [I]),
                 "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
                                               I, P]),
             }
@@ -167,6 +168,12 @@ def sgemm_config_info(cid: int):
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm_config_info")
     return name.value.decode(), dict(zip(PARAM_NAMES, list(params)))
+
+
+def sgemm_config_layouts(cid: int) -> int:
+    """1: configuration `cid` is built for every operand layout; 0: row-major
+    operands only; negative: an error status."""
+    return lib().sgemm_config_layouts(cid)
 
 
 def sgemm_force_config(cid: int) -> int:

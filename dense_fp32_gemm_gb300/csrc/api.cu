@@ -237,6 +237,9 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
   int id = g_forced.load();
   if (id < 0 || id >= kNumConfigs || (!row_major && !kConfigs[id]->all_layouts))
     id = choose_config(M, N, K);
+  // transposed operands need a configuration built for them (the tuner only
+  // picks such configurations; this guards a table written by hand)
+  if (!row_major && !kConfigs[id]->all_layouts) id = kIdWideBk32F2Ku16;
   const ConfigEntry& cfg = *kConfigs[id];
   const TileShape& S = cfg.shape;
 
@@ -494,6 +497,11 @@ SGEMM_API int sgemm_config_info(int id, char* name, int len, int* params) {
     for (int i = 0; i < 13; ++i) params[i] = v[i];
   }
   return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_config_layouts(int id) {
+  if (id < 0 || id >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
+  return kConfigs[id]->all_layouts ? 1 : 0;
 }
 
 SGEMM_API int sgemm_force_config(int id) {

@@ -1,7 +1,8 @@
 // cfg_wide_bk32_f2_ku32.cu -- instantiation of the FFMA kernel for CfgWideBk32F2Ku32 (one translation
-// unit per configuration so that the library compiles in parallel).
+// unit per configuration so that the library compiles in parallel). A
+// candidate of the tuner: built for every operand layout.
 #include "launch.cuh"
 
 namespace sgemm_gb300 {
-SGEMM_GB300_DEFINE_ENTRY(CfgWideBk32F2Ku32, kEntryWideBk32F2Ku32)
+SGEMM_GB300_DEFINE_ENTRY_ALL_LAYOUTS(CfgWideBk32F2Ku32, kEntryWideBk32F2Ku32)
 }  // namespace sgemm_gb300

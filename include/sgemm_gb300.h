@@ -207,6 +207,13 @@ int sgemm_config_info(int id, char* name, int len, int* params);
 int sgemm_force_config(int id);
 
 /*
+ * 1 when tile configuration `id` is built for every operand layout (op(A),
+ * op(B) in {N, T}; sgemm_ex and sgemm_strided_batched can use it), 0 when
+ * only for row-major A and B, SGEMM_ERR_INVALID_VALUE for an unknown id.
+ */
+int sgemm_config_layouts(int id);
+
+/*
  * The configuration sgemm() picks by itself for an M x N x K problem (the
  * tuned table's entry for the problem's shape class, ignoring
  * sgemm_force_config). *shape_class (if not NULL) receives the class:

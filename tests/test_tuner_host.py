@@ -32,3 +32,18 @@ def test_committed_table_is_well_formed():
     text = open(os.path.join(os.path.dirname(tune.__file__), "csrc", "tuned_table.inc")).read()
     rows = re.findall(r"X\((\w+), (\w+)\)", text)
     assert sorted(r[0] for r in rows) == sorted(tune.CLASS_TOKENS.values())
+
+
+def test_pick_winners_only_among_eligible():
+    t = {"k_dominant": {"A_x": [1.0], "B_x": [2.0]}}
+    assert tune.pick_winners(t, eligible={"B_x"}) == {"k_dominant": "B_x"}
+
+
+def test_every_class_dispatches_to_an_all_layout_configuration():
+    # the dispatcher's choice also serves sgemm_ex and sgemm_strided_batched
+    # with transposed operands, so it must be built for every layout
+    for cls, shapes in tune.CLASS_SHAPES.items():
+        for M, N, K, _, _ in shapes:
+            cid, _ = binding.sgemm_choose_config(M, N, K)
+            assert binding.sgemm_config_layouts(cid) == 1, (cls, binding.sgemm_config_info(cid)[0])
+    assert binding.sgemm_config_layouts(binding.sgemm_config_count()) == binding.SGEMM_ERR_INVALID_VALUE
