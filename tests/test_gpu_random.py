@@ -2,7 +2,8 @@
 pointer offsets, alpha and beta (zero included), input distributions,
 operand forms, batch counts, forced tile configurations, and each entry point
 (sgemm, sgemm_ex, sgemm_strided_batched, sgemm_3xtf32 in both kernel forms,
-sgemm_ladder). Every case is a fixed function of its index, so a failure
+sgemm_ladder, sgemm_noalloc, and sgemm_host on pinned or pageable host
+memory). Every case is a fixed function of its index, so a failure
 names a reproducible case. Padding holds NaN: a read outside an operand
 shows up in the result."""
 import numpy as np
@@ -18,8 +19,8 @@ import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
 N_, T_ = binding.SGEMM_OP_N, binding.SGEMM_OP_T
-CASES = 160
-ENTRIES = ["sgemm", "sgemm_ex", "batched", "tf32x3", "ladder"]
+CASES = 420
+ENTRIES = ["sgemm", "sgemm_ex", "batched", "tf32x3", "ladder", "noalloc", "host"]
 
 
 def _case(i):
@@ -45,6 +46,7 @@ def _case(i):
         cluster=int(r.integers(1, 3)),
         kernel=int(r.choice(binding.LADDER_KERNELS)),
         seed=int(r.integers(0, 2**31 - 1)),
+        pinned=bool(r.integers(0, 2)),
     )
 
 
@@ -89,13 +91,25 @@ def test_random_case(i):
         for j, p in enumerate(parts):
             out[j * stride: j * stride + p.size] = p.reshape(-1)
         return torch.from_numpy(out)
-    _, dA = H.device_buffer(flat(As, sA), c["offsets"][0])
-    _, dB = H.device_buffer(flat(Bs, sB), c["offsets"][1])
-    _, dC = H.device_buffer(flat(Cs, sC), c["offsets"][2])
+    e = c["entry"]
+    if e == "host":
+        def host_buffer(t, off):
+            store = torch.full((t.numel() + off + 16,), float("nan"))
+            if c["pinned"]:
+                store = store.pin_memory()
+            view = store[off: off + t.numel()]
+            view.copy_(t)
+            return store, view
+        _, dA = host_buffer(flat(As, sA), c["offsets"][0])
+        _, dB = host_buffer(flat(Bs, sB), c["offsets"][1])
+        _, dC = host_buffer(flat(Cs, sC), c["offsets"][2])
+    else:
+        _, dA = H.device_buffer(flat(As, sA), c["offsets"][0])
+        _, dB = H.device_buffer(flat(Bs, sB), c["offsets"][1])
+        _, dC = H.device_buffer(flat(Cs, sC), c["offsets"][2])
     s = torch.cuda.current_stream().cuda_stream
     pA, pB, pC = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
     alpha, beta = c["alpha"], c["beta"]
-    e = c["entry"]
     if e in ("sgemm", "sgemm_ex", "batched"):
         assert binding.sgemm_force_config(c["config"]) == 0
     prev_cluster = binding.sgemm_3xtf32_set_cluster_size(c["cluster"])
@@ -110,16 +124,21 @@ def test_random_case(i):
                                                ldb, sB, beta, pC, ldc, sC, batch, s)
         elif e == "tf32x3":
             st = binding.sgemm_3xtf32(M, N, K, alpha, pA, lda, pB, ldb, beta, pC, ldc, s)
+        elif e == "noalloc":
+            st = binding.sgemm_noalloc(M, N, K, alpha, pA, lda, pB, ldb, beta, pC, ldc, s)
+        elif e == "host":
+            st = binding.sgemm_host(M, N, K, alpha, pA, lda, pB, ldb, beta, pC, ldc, s)
         else:
             st = binding.sgemm_ladder(c["kernel"], M, N, K, alpha, pA, lda, pB, ldb, beta, pC, ldc,
                                       s)
         assert st == 0, f"case {c}: {binding.sgemm_status_string(st)}"
-        assert binding.sgemm_poll_device_status(s) == (0, 0)
         torch.cuda.synchronize()
+        if e != "noalloc":  # its status lives in its own buffer
+            assert binding.sgemm_poll_device_status(s) == (0, 0)
     finally:
         binding.sgemm_force_config(-1)
         binding.sgemm_3xtf32_set_cluster_size(prev_cluster)
-    out = dC.cpu().numpy()
+    out = dC.cpu().numpy() if e != "host" else dC.numpy()
     w = Workload(f"random{i}", M, N, K, alpha, beta, c["dist"], c["seed"])
     for j, (A2, B2, C2) in enumerate(mats):
         got = out[j * sC: j * sC + Cs[j].size].reshape(M, ldc)
