@@ -164,6 +164,10 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   constexpr int A_ST = a_stage_floats(S), B_ST = b_stage_floats(S);
   static_assert(BK * AP <= A_ST && BK * BP <= B_ST, "stage sizes");
   constexpr int D = ST - 2;                    // k-slices loaded ahead
+  // k-step of a slice's last chunk at which the copies of a later slice are
+  // issued when D >= 2 (always inside the chunk, so exactly once per slice)
+  constexpr int kIssueAt = KU > 4 ? 4 : 0;
+  static_assert(kIssueAt < KU, "issue point inside the last chunk");
   constexpr int LANES_N = WSUBN / TN;          // lanes along n in a sub-tile
   constexpr int RM = WMITER * TM, RN = WNITER * TN;  // a lane's rows / cols
   constexpr int A_ROWS = NT / kAloadK;         // rows per transposing-copy pass
@@ -447,12 +451,12 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   }
 
   for (int step = 0; step < nsteps && !aborted; ++step) {
-    if (issued < nsteps) {
-      if (!issue_next()) {
-        aborted = true;
-        break;
-      }
-    }
+    // With two or more slices in flight ahead (D >= 2), the copies for a later
+    // step are issued a few k-steps into this one, so that the step's FMAs
+    // start without waiting behind them; with one (D == 1) that slice is the
+    // next one, so its copies go out first to have the whole step to land.
+    bool issue_ok = true;
+    if (D < 2 && issued < nsteps) issue_ok = issue_next();
     const int slot = step % ST;
     const float* a_s = As + slot * A_ST + a_frag_off;
     const float* b_s = Bs + slot * B_ST + b_frag_off;
@@ -517,6 +521,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 #pragma unroll
       for (int kk = 0; kk < KU; ++kk) {
         const int cur = kk & 1;
+        if (D >= 2 && kk == kIssueAt && issued < nsteps) issue_ok = issue_next();
         if (kk + 1 < KU) {
           load_frags(cur ^ 1, a_s + (kc + kk + 1) * AP, b_s + (kc + kk + 1) * BP);
           if (kk == KU / 2 - 1 && has_next) ready = test_full(step + 1);
@@ -532,7 +537,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     // release the slot: one arrival per warp once all its lanes are done
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bb->empty[slot]));
-    if (!next_ok) {
+    if (!next_ok || !issue_ok) {
       aborted = true;
       break;
     }
