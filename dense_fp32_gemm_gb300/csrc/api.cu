@@ -24,6 +24,13 @@
 #define SGEMM_API extern "C" __attribute__((visibility("default")))
 
 namespace sgemm_gb300 {
+
+// The kernel for very small problems (tiny.cu).
+bool tiny_wanted(int M, int N, int K);
+cudaError_t tiny_launch(int dev, int M, int N, int K, float alpha, const float* A, long long lda,
+                        const float* B, long long ldb, float beta, float* C, long long ldc,
+                        cudaStream_t stream, char* text, int text_len);
+
 namespace {
 
 // ---- configuration registry -------------------------------------------------
@@ -235,6 +242,16 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
 
   const bool row_major = (opA == SGEMM_OP_N && opB == SGEMM_OP_N);
   int id = g_forced.load();
+  // very small row-major problems: the latency-first kernel (tiny.cu), unless
+  // a tile configuration is forced
+  if (id < 0 && row_major && batch == 1 && tiny_wanted(M, N, K)) {
+    if (tiny_launch(dev, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, g_last_config,
+                    (int)sizeof(g_last_config)) != cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
+  }
   if (id < 0 || id >= kNumConfigs || (!row_major && !kConfigs[id]->all_layouts))
     id = choose_config(M, N, K);
   // transposed operands need a configuration built for them (the tuner only

@@ -51,7 +51,8 @@ struct KernelParams;
   X(MiniF2, 64, 64, 16, 32, 64, 2, 4, 4, 64, 3, 6, 8, 2)              \
   X(SmallF2, 64, 128, 16, 32, 64, 2, 4, 4, 128, 3, 3, 8, 2)               \
   X(WideBk32F2Ku32, 128, 256, 32, 64, 64, 2, 4, 4, 256, 4, 1, 32, 2)      \
-  X(FlatBk24F2Ku24, 64, 256, 24, 64, 64, 2, 4, 4, 128, 3, 2, 24, 2)
+  X(FlatBk24F2Ku24, 64, 256, 24, 64, 64, 2, 4, 4, 128, 3, 2, 24, 2)       \
+  X(MidBk32F2Ku32, 128, 64, 32, 64, 32, 2, 4, 4, 128, 4, 2, 32, 2)
 
 #define SGEMM_GB300_CFG_STRUCT(NAME, BM, BN, BK, WM, WN, WNI, TM, TN, NT, ST, MINB, KU, OR)     \
   struct Cfg##NAME {                                                                            \
