@@ -17,6 +17,7 @@ sample of the same workload; it runs on rank 0 only.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import datetime as _dt
 import functools
 import glob
@@ -120,6 +121,17 @@ def profiled_traffic(workload, tile_config):
     if not c or not tile_config.startswith(c.group(1)):
         return None
     return float(m.group(1))
+
+
+# ---- NVTX ranges: name the bench's phases in profiler timelines ------------------------
+@contextlib.contextmanager
+def nvtx_range(name):
+    import torch
+    torch.cuda.nvtx.range_push(name)
+    try:
+        yield
+    finally:
+        torch.cuda.nvtx.range_pop()
 
 
 # ---- clocks -------------------------------------------------------------------------
@@ -325,9 +337,10 @@ def run_ours(args, w):
     sampler = ClockSampler(gpu_id) if rank == 0 else None
     time.sleep(1.0 if sampler else 0.0)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+    with nvtx_range("warmup"):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
     st, detail = binding.sgemm_poll_device_status(sh)
     if st != 0:
         raise RuntimeError(f"device status {st} detail {detail} after warm-up")
@@ -340,13 +353,14 @@ def run_ours(args, w):
     t_wall0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    with nvtx_range("timed_steps"):
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
     barrier(world)
     t_wall1 = time.time()
     total_s = start.elapsed_time(end) / 1e3
@@ -374,11 +388,12 @@ def run_ours(args, w):
         barrier(world)
         torch.cuda.synchronize(dev)
         s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s3.record(stream)
-        for _ in range(args.steps):
-            step3()
-        e3.record(stream)
-        torch.cuda.synchronize(dev)
+        with nvtx_range("tf32x3_steps"):
+            s3.record(stream)
+            for _ in range(args.steps):
+                step3()
+            e3.record(stream)
+            torch.cuda.synchronize(dev)
         t3 = max_over_ranks(s3.elapsed_time(e3) / 1e3, world)
         st, detail = binding.sgemm_poll_device_status(sh)
         if st != 0:
@@ -402,17 +417,18 @@ def run_ours(args, w):
                                  w.LDB, w.beta, hC.data_ptr(), w.LDC, sh)
         if st2 != 0:
             raise RuntimeError(f"sgemm_host: {binding.sgemm_status_string(st2)}")
-    for _ in range(2):
+    for _ in range(max(3, min(args.warmup, 10))):
         host_step()
     torch.cuda.synchronize(dev)
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        host_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    with nvtx_range("e2e_steps"):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            host_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
     e2e_value = aggregate(gemm_flops(w.M, w.N, w.K), e2e_steps, e2e_s, world)
     h2d_bytes = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if w.beta != 0 else 0))

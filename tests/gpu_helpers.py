@@ -20,16 +20,27 @@ REL_TOL = 1e-5
 ABS_FLOOR = 1e-30
 
 
+GUARD = 64  # NaN floats after every device buffer (and before it when offset)
+
+
 def device_buffer(host_flat: torch.Tensor, offset_floats: int = 0):
     """Copy a flat host buffer to the device, optionally starting
     `offset_floats` floats past a 256-byte aligned allocation (to exercise
-    unaligned pointers). Returns (storage tensor, view tensor)."""
+    unaligned pointers), with GUARD NaN floats after it. Returns (storage
+    tensor, view tensor)."""
     n = host_flat.numel()
-    store = torch.empty(n + offset_floats + 64, dtype=torch.float32, device="cuda")
+    store = torch.empty(n + offset_floats + GUARD, dtype=torch.float32, device="cuda")
     store.fill_(float("nan"))
     view = store[offset_floats: offset_floats + n]
     view.copy_(host_flat)
     return store, view
+
+
+def assert_guards_intact(store: torch.Tensor, offset_floats: int, n: int, what=""):
+    """The NaN floats before and after a buffer's view were not written."""
+    host = store.cpu().numpy()
+    before, after = host[:offset_floats], host[offset_floats + n:]
+    assert np.all(np.isnan(before)) and np.all(np.isnan(after)), f"{what}: a guard band was written"
 
 
 def run_cuda(w: Workload, A, B, C, offsets=(0, 0, 0), config=None, stream=None, check_status=True,
@@ -43,7 +54,7 @@ def run_cuda(w: Workload, A, B, C, offsets=(0, 0, 0), config=None, stream=None, 
     _, dB = device_buffer(B, offsets[1])
     if C is None:
         C = torch.full((w.M * w.LDC,), float("nan"))
-    _, dC = device_buffer(C, offsets[2])
+    storeC, dC = device_buffer(C, offsets[2])
     if config is not None:
         assert binding.sgemm_force_config(config) == 0
     try:
@@ -58,6 +69,7 @@ def run_cuda(w: Workload, A, B, C, offsets=(0, 0, 0), config=None, stream=None, 
     finally:
         if config is not None:
             binding.sgemm_force_config(-1)
+    assert_guards_intact(storeC, offsets[2], C.numel(), what=f"{w.name} C")
     return dC.cpu().numpy()
 
 

@@ -40,7 +40,7 @@ def _run_ex(w, opA, opB, offsets=(0, 0, 0), ld_pad=(0, 0, 0), config=None):
     ldc = w.N + ld_pad[2]
     _, dA = H.device_buffer(torch.from_numpy(Af), offsets[0])
     _, dB = H.device_buffer(torch.from_numpy(Bf), offsets[1])
-    _, dC = H.device_buffer(torch.from_numpy(Cf.reshape(-1)), offsets[2])
+    storeC, dC = H.device_buffer(torch.from_numpy(Cf.reshape(-1)), offsets[2])
     if config is not None:
         binding.sgemm_force_config(config)
     try:
@@ -52,6 +52,7 @@ def _run_ex(w, opA, opB, offsets=(0, 0, 0), ld_pad=(0, 0, 0), config=None):
         torch.cuda.synchronize()
     finally:
         binding.sgemm_force_config(-1)
+    H.assert_guards_intact(storeC, offsets[2], Cf.size, what="sgemm_ex C")
     got = dC.cpu().numpy().reshape(w.M, ldc)
     ref, mag = oracle.sgemm(A2, B2, None if w.beta == 0 else C.numpy().reshape(w.M, w.LDC)[:, : w.N],
                             w.alpha, w.beta)

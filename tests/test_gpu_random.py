@@ -106,7 +106,7 @@ def test_random_case(i):
     else:
         _, dA = H.device_buffer(flat(As, sA), c["offsets"][0])
         _, dB = H.device_buffer(flat(Bs, sB), c["offsets"][1])
-        _, dC = H.device_buffer(flat(Cs, sC), c["offsets"][2])
+        storeC, dC = H.device_buffer(flat(Cs, sC), c["offsets"][2])
     s = torch.cuda.current_stream().cuda_stream
     pA, pB, pC = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
     alpha, beta = c["alpha"], c["beta"]
@@ -138,6 +138,8 @@ def test_random_case(i):
     finally:
         binding.sgemm_force_config(-1)
         binding.sgemm_3xtf32_set_cluster_size(prev_cluster)
+    if e != "host":
+        H.assert_guards_intact(storeC, c["offsets"][2], dC.numel(), what=f"case {c}")
     out = dC.cpu().numpy() if e != "host" else dC.numpy()
     w = Workload(f"random{i}", M, N, K, alpha, beta, c["dist"], c["seed"])
     for j, (A2, B2, C2) in enumerate(mats):
