@@ -74,8 +74,22 @@ TF32_OVER_BF16 = 1.1 / 2.25
 
 
 def tf32x3_peak_tflops(peaks):
+    """The 3xTF32 roof estimated from the measured BF16 peak (TF32 runs at
+    half the BF16 rate, nominally), three TF32 products per FP32 product."""
     bf16 = peaks.get("bf16_tflops")
     return (float(bf16) * TF32_OVER_BF16 / 3.0) if bf16 else None
+
+
+def tf32x3_roof(binding, peaks):
+    """(roof TFLOP/s, basis, measured TF32 TFLOP/s or None): the measured
+    tcgen05 kind::tf32 throughput of this device / 3 (the library's probe
+    kernel), else the BF16-derived estimate."""
+    st, tf32 = binding.sgemm_diag_tf32_mma_rate(20000)
+    if st == 0 and tf32 > 0:
+        return (tf32 / 3.0, "measured tcgen05.mma kind::tf32 throughput (probe kernel, one CTA "
+                            "per SM, burst) / 3 TF32 products per FP32 product", tf32)
+    return (tf32x3_peak_tflops(peaks), "measured bf16 peak x 1.1/2.25 (TF32/BF16 nominal) / 3 "
+                                       "TF32 products per FP32 product", None)
 
 
 # The sources that define the FFMA kernel the bench times and how it is
@@ -465,13 +479,15 @@ def run_ours(args, w):
         "clocks": clocks,
     }
     if tf32x3 is not None:
-        p3 = tf32x3_peak_tflops(peaks)
+        p3, basis, tf32_measured = tf32x3_roof(binding, peaks)
         a3 = tf32x3["value"] / 1e3
+        est = tf32x3_peak_tflops(peaks)
         tf32x3["roofline"] = {"bound": "tensor", "achieved": round(a3, 3),
                               "peak": round(p3, 3) if p3 else None, "unit": "TFLOP/s",
-                              "frac": round(a3 / p3, 4) if p3 else None,
-                              "peak_basis": "measured bf16 peak x 1.1/2.25 (TF32/BF16 nominal) / 3 "
-                                            "TF32 products per FP32 product"}
+                              "frac": round(a3 / p3, 4) if p3 else None, "peak_basis": basis,
+                              "tf32_mma_tflops_measured": (round(tf32_measured, 1)
+                                                           if tf32_measured else None),
+                              "peak_from_bf16_estimate": round(est, 3) if est else None}
         line["tf32x3"] = tf32x3
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, C, budget_s=args.cpu_budget)
@@ -558,7 +574,7 @@ def run_report(args):
     peaks = measured_peaks()
     max_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
     peak_tf = ffma_peak_tflops(props.multi_processor_count, max_mhz)
-    p3 = tf32x3_peak_tflops(peaks)
+    p3, _, _ = tf32x3_roof(binding, peaks)
     s = torch.cuda.current_stream().cuda_stream
     flush = _l2_flusher()
     for name in REPORT_WORKLOADS:

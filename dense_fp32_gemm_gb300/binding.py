@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_3xtf32_set_cluster_size": (I, [I]),
                 "sgemm_host_set_pipeline": (I, [I, I, I, I]),
                 "sgemm_config_layouts": (I, [I]),
+                "sgemm_diag_tf32_mma_rate": (I, [I, ctypes.POINTER(ctypes.c_double)]),
                 "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
                                               I, P]),
             }
@@ -168,6 +169,14 @@ def sgemm_config_info(cid: int):
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm_config_info")
     return name.value.decode(), dict(zip(PARAM_NAMES, list(params)))
+
+
+def sgemm_diag_tf32_mma_rate(iters: int = 20000):
+    """(status, TFLOP/s): the measured TF32 tensor-core throughput of the
+    current device (synchronous, about 6 ms)."""
+    v = ctypes.c_double(0.0)
+    st = lib().sgemm_diag_tf32_mma_rate(iters, ctypes.byref(v))
+    return st, v.value
 
 
 def sgemm_config_layouts(cid: int) -> int:

@@ -262,6 +262,18 @@ int sgemm_diag_wait_timeout(long long timeout_ns, void* stream);
 long long sgemm_set_wait_timeout_ns(long long ns);
 
 /*
+ * Diagnostic: the TF32 tensor-core throughput of the current device, in
+ * TFLOP/s, measured. One CTA per SM issues `iters` x 4 back-to-back
+ * tcgen05.mma.kind::tf32 of M 128, N 256, K 8 from shared memory into tensor
+ * memory, with no loads in the loop; the launch is timed with CUDA events
+ * (about 6 ms at iters = 20000 on GB300). Synchronous. The 3xTF32 path's
+ * roofline divides this by three. Returns SGEMM_ERR_INVALID_VALUE for iters
+ * < 1 or a NULL result pointer, SGEMM_ERR_DEVICE_TIMEOUT if the MMAs did not
+ * complete within 4 s.
+ */
+int sgemm_diag_tf32_mma_rate(int iters, double* tflops);
+
+/*
  * The same C = alpha * A * B + beta * C as sgemm(), with the same arguments,
  * checks and results, for callers that must not allocate device memory: code
  * running while a stream is captured into a graph, applications whose memory

@@ -78,3 +78,8 @@ def test_config_registry():
     assert len(names) == n
     assert binding.sgemm_force_config(n) == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_force_config(-1) == 0
+
+
+def test_tf32_rate_probe_rejects_bad_arguments():
+    # checked on the host before any device call
+    assert binding.sgemm_diag_tf32_mma_rate(0)[0] == binding.SGEMM_ERR_INVALID_VALUE
