@@ -79,7 +79,10 @@ typedef enum {
  * C by beta without reading A or B. beta == 0 never reads C, so C may hold
  * NaN or garbage. A and B may have any 4-byte alignment (the 128-bit and TMA
  * paths are used only when alignment allows). C must not overlap A or B.
- * stream: a cudaStream_t (NULL = legacy default stream).
+ * stream: a cudaStream_t (NULL = legacy default stream). Problems with
+ * M * N * K <= 2^25 run a latency-first kernel (one CTA per 32 x 32 tile, no
+ * K-split) unless a tile configuration is forced; larger ones the persistent
+ * kernel with the tuned configuration of their shape class.
  */
 int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
           float beta, float* C, int ldc, void* stream);
@@ -292,7 +295,8 @@ int sgemm_diag_tf32_mma_rate(int iters, double* tflops);
  * GPU (other streams, other host threads) race and must not be issued. The
  * device status of these calls is kept in the array and cleared by the next
  * call; sgemm_poll_device_status() does not report it. The tile configuration
- * is always the automatic choice (sgemm_force_config() does not apply).
+ * is always the automatic choice (sgemm_force_config() does not apply), and
+ * problems with M * N * K <= 2^25 run the same tiny-problem kernel as sgemm().
  */
 int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
                   int ldb, float beta, float* C, int ldc, void* stream);
