@@ -77,7 +77,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_ex": (I, [I, I, I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_host": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_ladder": (I, [I, I, I, I, F, P, I, P, I, F, P, I, P]),
-                "sgemm_3xtf32_set_cluster_size": (I, [I]),
+                "sgemm_3xtf32_set_kernel_form": (I, [I]),
                 "sgemm_host_set_pipeline": (I, [I, I, I, I]),
                 "sgemm_config_layouts": (I, [I]),
                 "sgemm_diag_tf32_mma_rate": (I, [I, ctypes.POINTER(ctypes.c_double)]),
@@ -260,10 +260,15 @@ def sgemm_ladder(kernel, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=No
 LADDER_KERNELS = (3, 7, 8)
 
 
-def sgemm_3xtf32_set_cluster_size(cluster_size: int) -> int:
-    """2: sgemm_3xtf32 runs CTA pairs sharing B tiles by multicast (default);
-    1: single CTAs. Returns the previous setting (or an error status)."""
-    return lib().sgemm_3xtf32_set_cluster_size(cluster_size)
+SGEMM_X3_SINGLE, SGEMM_X3_PAIR, SGEMM_X3_PAIR_MULTICAST = 1, 2, 3
+X3_FORMS = (SGEMM_X3_PAIR, SGEMM_X3_PAIR_MULTICAST, SGEMM_X3_SINGLE)
+
+
+def sgemm_3xtf32_set_kernel_form(form: int) -> int:
+    """SGEMM_X3_PAIR (default): CTA pairs with two-SM MMAs; SGEMM_X3_PAIR_MULTICAST:
+    CTA pairs sharing B tiles by multicast; SGEMM_X3_SINGLE: single CTAs.
+    Returns the previous setting (or an error status)."""
+    return lib().sgemm_3xtf32_set_kernel_form(form)
 
 
 # ---- torch conveniences (marshalling only) ------------------------------------------

@@ -57,6 +57,7 @@ enum DeviceStatus : int {
   kDevTimeoutEmpty = 2,   // a slot was never released by its consumers
   kDevTimeoutFlag = 3,    // a split partial was never published
   kDevTimeoutSync = 4,    // a CTA-wide rendezvous did not complete
+  kDevTmemMismatch = 5,   // the two CTAs of a two-SM pair got different TMEM columns
 };
 
 struct KernelParams {

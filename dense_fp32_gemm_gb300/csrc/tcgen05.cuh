@@ -10,18 +10,38 @@ namespace tc {
 
 // ---- tensor memory (TMEM) allocation: one full warp executes these -------
 // Allocates `ncols` columns (a power of two >= 32) of all 128 lanes; the
-// TMEM address is written to shared memory at `dst_smem`.
+// TMEM address is written to shared memory at `dst_smem`. CG = 2 (the pair
+// form of the MMA, whose accumulator spans the TMEM of two CTAs): one warp
+// of each CTA of the pair executes it, and both get the same columns. Every
+// tcgen05 instruction of a kernel uses the same CG.
+template <int CG = 1>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
 }
+template <int CG = 1>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
+template <int CG = 1>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
 
 // ---- ordering of tensor-core work around thread synchronisation ----------
@@ -61,6 +81,38 @@ __device__ __forceinline__ void commit_multicast(uint32_t mbar_smem, uint16_t ct
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(mbar_smem),
       "h"(cta_mask)
+      : "memory");
+}
+
+// ---- the pair form (cta_group::2) ------------------------------------------
+// D[tmem] (+)= A * B for an M = 256 tile spread over a CTA pair, issued by one
+// thread of the even CTA: A rows 0-127 come from that CTA's shared memory and
+// rows 128-255 from the odd CTA's, at the same offset (a_desc); B's N columns
+// likewise in two halves (b_desc); D rows 0-127 land in the even CTA's TMEM,
+// rows 128-255 in the odd CTA's, at the same TMEM address.
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Commit of the pair form: arrives on the mbarrier at offset `mbar_smem` of
+// every CTA in `cta_mask` (or of this CTA only) when the MMAs issued so far
+// have completed.
+__device__ __forceinline__ void commit_pair_multicast(uint32_t mbar_smem, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(mbar_smem),
+      "h"(cta_mask)
+      : "memory");
+}
+__device__ __forceinline__ void commit_pair(uint32_t mbar_smem) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          mbar_smem)
       : "memory");
 }
 

@@ -78,29 +78,40 @@ constexpr int BM = 128, BN = 256, NT = 320;
 // 96 KB stages, 128-byte swizzle) has half the per-stage hand-offs. Measured
 // on GB300: 16 is faster from K = 1024 up (4096^3: 251 against 226 TFLOP/s),
 // 32 below (8191 x 1000 x 777: 99 against 86 TFLOP/s).
-template <int BK_>
+// B_PARTS = 2 (the two-SM form): a CTA holds half of each B tile.
+template <int BK_, int B_PARTS = 1>
 struct Slice {
   static constexpr int BK = BK_;
   static_assert(BK == 32 || BK == 16, "k-slice width");
   static constexpr int ROW_BYTES = BK * 4;
-  static constexpr int ST = 64 / BK;
   static constexpr int A_BYTES = BM * BK * 4;                      // one of A_hi, A_lo
-  static constexpr int B_BYTES = BN * BK * 4;                      // one of B_hi, B_lo
+  static constexpr int B_BYTES = BN / B_PARTS * BK * 4;            // one of B_hi, B_lo
   // a stage: [A_hi | A_lo | B_hi | B_lo]; TMA writes the _hi tiles (the raw
   // values), the converter warps the _lo tiles
-  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 or 48 KB
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 / 48 KB, or 64 / 32 KB
+  static constexpr int ST = 192 * 1024 / STAGE_BYTES;              // 2 / 4, or 3 / 6
 };
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kStageRegion = 192 * 1024;
 static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
-                  Slice<32>::ST * Slice<32>::STAGE_BYTES == kStageRegion,
-              "both widths fill the same stage region");
+                  Slice<32>::ST * Slice<32>::STAGE_BYTES == kStageRegion &&
+                  Slice<16, 2>::ST * Slice<16, 2>::STAGE_BYTES == kStageRegion &&
+                  Slice<32, 2>::ST * Slice<32, 2>::STAGE_BYTES == kStageRegion &&
+                  Slice<16, 2>::ST <= kMaxStages,
+              "every width fills the same stage region");
 constexpr int ACC_COLS = BN;              // one FP32 accumulator: 128 lanes x BN columns
-constexpr int TMEM_COLS = 2 * ACC_COLS;   // two, so the epilogue overlaps the next MMAs
+constexpr int NBUF = 2;                   // accumulators, so the epilogue overlaps the next MMAs
+constexpr int TMEM_COLS = NBUF * ACC_COLS;  // all 512 columns
+// Kernel forms (the values sgemm_3xtf32_set_kernel_form takes): single CTAs;
+// CTA pairs whose even CTA issues M = 256 MMAs over both (cta_group::2),
+// each CTA holding half of every B tile; CTA pairs that share B tiles by
+// multicast, each CTA issuing its own M = 128 MMAs.
+enum Form : int { kSingle = 1, kTwoSmPair = 2, kMulticastPair = 3 };
 constexpr int EPI_THREADS = 128;          // warps 2-5
 constexpr int CONV_WARP0 = 6;             // warps 6-9 write the residual tiles
 constexpr int CONV_THREADS = 128;
 constexpr uint32_t IDESC = tc::idesc_tf32(BM, BN);
+constexpr uint32_t IDESC_PAIR = tc::idesc_tf32(2 * BM, BN);  // M = 256 over a CTA pair
 static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
 
 struct Barriers {
@@ -187,7 +198,18 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc
   }
 }
 
-template <int CL, int BK>
+// bounded_wait for a barrier that threads of the peer CTA arrive on: the
+// polling is CTA-scoped (cheap); once the phase is seen complete, one more
+// test of the same phase acquires at cluster scope. The phase cannot move on
+// in between: its next completion needs work this thread has not issued yet.
+__device__ __forceinline__ bool bounded_wait_cluster(uint32_t bar, uint32_t parity,
+                                                     volatile int* abort_w, int* status, int code,
+                                                     long long timeout_ns) {
+  if (!bounded_wait(bar, parity, abort_w, status, code, timeout_ns)) return false;
+  return ptx::mbar_try_wait_cluster(bar, parity);
+}
+
+template <int FORM, int BK>
 __global__ void __launch_bounds__(NT, 1)
     gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB) {
@@ -199,8 +221,11 @@ __global__ void __launch_bounds__(NT, 1)
   volatile int* abort_w = &bar->abort;
   const uint32_t base_addr = ptx::smem_addr(base);
 
-  static_assert(CL == 1 || CL == 2, "cluster size");
-  using S = Slice<BK>;
+  static_assert(FORM == kSingle || FORM == kMulticastPair || FORM == kTwoSmPair, "form");
+  constexpr bool TWO_SM = FORM == kTwoSmPair;
+  constexpr int CL = FORM == kSingle ? 1 : 2;       // CTAs per cluster
+  constexpr int CG = TWO_SM ? 2 : 1;                // cta_group of every tcgen05 instruction
+  using S = Slice<BK, TWO_SM ? 2 : 1>;
   constexpr int ST = S::ST, ROW_BYTES = S::ROW_BYTES;
   constexpr int A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES, STAGE_BYTES = S::STAGE_BYTES;
   constexpr uint16_t kPair = 0x3;  // both CTAs of a cluster of two
@@ -213,14 +238,19 @@ __global__ void __launch_bounds__(NT, 1)
   const int npieces = num_pieces(sc, b);
 
   if (tid == 0) {
+    // two-SM form: the even CTA's MMA thread waits on its own conv barrier
+    // (its converter warps, plus one relayed arrival for the odd CTA's) and
+    // tmem_empty barriers (the epilogue warps of both CTAs), and its commits
+    // arrive on the empty and tmem_full barriers of both
     for (int s = 0; s < ST; ++s) {
       ptx::mbar_init(ptx::smem_addr(&bar->full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&bar->conv[s]), CONV_THREADS / 32);
-      ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), CL);
+      ptx::mbar_init(ptx::smem_addr(&bar->conv[s]),
+                     CONV_THREADS / 32 + ((TWO_SM && rank == 0) ? 1 : 0));
+      ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), TWO_SM ? 1 : CL);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_addr(&bar->tmem_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&bar->tmem_empty[i]), 4);
+      ptx::mbar_init(ptx::smem_addr(&bar->tmem_empty[i]), (TWO_SM ? 2 : 1) * 4);
     }
     ptx::mbar_init(ptx::smem_addr(&bar->drain), 1);
     ptx::mbar_init(ptx::smem_addr(&bar->epi_sync), EPI_THREADS);
@@ -230,8 +260,8 @@ __global__ void __launch_bounds__(NT, 1)
     ptx::tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tc::tmem_alloc(ptx::smem_addr(&bar->tmem_addr), TMEM_COLS);
-    tc::tmem_relinquish();
+    tc::tmem_alloc<CG>(ptx::smem_addr(&bar->tmem_addr), TMEM_COLS);
+    tc::tmem_relinquish<CG>();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -239,6 +269,16 @@ __global__ void __launch_bounds__(NT, 1)
   if (CL == 2) ptx::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem = bar->tmem_addr;
+  if (TWO_SM && tid == 0) {
+    // the MMAs of the pair write the same TMEM address in both CTAs
+    const uint32_t peer = ptx::ld_shared_cluster(
+        ptx::mapa(ptx::smem_addr(&bar->tmem_addr), (uint32_t)(rank ^ 1)));
+    if (peer != tmem) {
+      *abort_w = 1;
+      atomicCAS(p.status, 0, (int)kDevTmemMismatch);
+    }
+  }
+  if (TWO_SM) __syncthreads();  // every role sees the abort word
 
   if (warp == 0) {
     // ---- TMA producer: the raw A and B^T tiles of every k-slice of every piece
@@ -264,6 +304,9 @@ __global__ void __launch_bounds__(NT, 1)
           ptx::tma_load_2d(st0, &tmA, kb * BK, tm * BM, fb);
           if (CL == 1) {
             ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN, fb);
+          } else if (TWO_SM) {
+            // this CTA's half of the B tile (N columns 128 * rank ..), into this CTA
+            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN + rank * (BN / 2), fb);
           } else {
             // this CTA's half of the B tile, into both CTAs
             const uint32_t half = (uint32_t)(rank * (B_BYTES / 2));
@@ -282,8 +325,9 @@ __global__ void __launch_bounds__(NT, 1)
           if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
       }
       if (CL == 2) {
-        // the peer's MMA warp arrives on this CTA's empty barriers: wait
-        // (bounded) for its arrivals on the last use of every stage
+        // the peer's MMA warp (the even CTA's, in the two-SM form) arrives on
+        // this CTA's empty barriers: wait (bounded) for its arrivals on the
+        // last use of every stage
         for (int j = it; j < it + ST; ++j) {
           const uint32_t eb = ptx::smem_addr(&bar->empty[j % ST]);
           while (!ptx::mbar_try_wait(eb, (uint32_t)((j / ST) & 1) ^ 1u))
@@ -292,27 +336,58 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: piece i accumulates into TMEM columns (i % 2) * BN ------
-    if (lane == 0) {
+    // ---- two-SM form, odd CTA: relays each stage's conv completion to the
+    // even CTA with one remote arrival. (Measured on GB300: one relayed
+    // arrival per stage runs 26 % faster at 4096^3 than an arrival from each
+    // converter warp of the odd CTA.)
+    if (TWO_SM && rank != 0 && lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int i = 0; i < npieces && ok && !*abort_w; ++i) {
+        const Piece pc = get_piece(sc, b, i);
+        for (int kb = pc.kb; kb < pc.ke; ++kb, ++it) {
+          const int s = it % ST;
+          ok = bounded_wait(ptx::smem_addr(&bar->conv[s]), (uint32_t)((it / ST) & 1), abort_w,
+                            p.status, kDevTimeoutFull, p.timeout_ns);
+          if (!ok) break;
+          ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_addr(&bar->conv[s]), 0u));
+        }
+      }
+    }
+    // ---- MMA issuer: piece i accumulates into TMEM columns (i % NBUF) * BN.
+    // In the two-SM form the even CTA issues for the pair.
+    if (lane == 0 && (!TWO_SM || rank == 0)) {
       int it = 0;
       bool issued_any = false;
       for (int i = 0; i < npieces && !*abort_w; ++i) {
         const Piece pc = get_piece(sc, b, i);
-        const int buf = i & 1;
+        const int buf = i % NBUF;
         const uint32_t d = tmem + (uint32_t)(buf * ACC_COLS);
-        // the epilogue must have read this accumulator's previous piece
-        if (!bounded_wait(ptx::smem_addr(&bar->tmem_empty[buf]), (uint32_t)((i >> 1) & 1) ^ 1u,
-                          abort_w, p.status, kDevTimeoutSync, p.timeout_ns))
+        // the epilogue (of both CTAs, in the two-SM form) must have read this
+        // accumulator's previous piece
+        const uint32_t eb = ptx::smem_addr(&bar->tmem_empty[buf]);
+        const uint32_t epar = (uint32_t)((i / NBUF) & 1) ^ 1u;
+        if (!(TWO_SM ? bounded_wait_cluster(eb, epar, abort_w, p.status, kDevTimeoutSync,
+                                            p.timeout_ns)
+                     : bounded_wait(eb, epar, abort_w, p.status, kDevTimeoutSync, p.timeout_ns)))
           break;
         tc::fence_after_sync();
         bool ok = true;
         for (int kb = pc.kb; kb < pc.ke; ++kb, ++it) {
           const int s = it % ST;
-          // the raw tiles (TMA) and the residual tiles (converter warps)
-          if (!bounded_wait(ptx::smem_addr(&bar->full[s]), (uint32_t)((it / ST) & 1), abort_w,
-                            p.status, kDevTimeoutFull, p.timeout_ns) ||
-              !bounded_wait(ptx::smem_addr(&bar->conv[s]), (uint32_t)((it / ST) & 1), abort_w,
-                            p.status, kDevTimeoutFull, p.timeout_ns)) {
+          const uint32_t par = (uint32_t)((it / ST) & 1);
+          // the raw tiles (TMA) and the residual tiles (converter warps). In
+          // the two-SM form this CTA's conv barrier completes once the
+          // converters of both CTAs are done, each only after its own CTA's
+          // raw tiles landed.
+          const bool ready =
+              TWO_SM ? bounded_wait_cluster(ptx::smem_addr(&bar->conv[s]), par, abort_w, p.status,
+                                            kDevTimeoutFull, p.timeout_ns)
+                     : (bounded_wait(ptx::smem_addr(&bar->full[s]), par, abort_w, p.status,
+                                     kDevTimeoutFull, p.timeout_ns) &&
+                        bounded_wait(ptx::smem_addr(&bar->conv[s]), par, abort_w, p.status,
+                                     kDevTimeoutFull, p.timeout_ns));
+          if (!ready) {
             ok = false;
             break;
           }
@@ -327,23 +402,38 @@ __global__ void __launch_bounds__(NT, 1)
             const uint64_t b_lo =
                 tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + 2 * A_BYTES + B_BYTES + koff);
             const uint32_t first = (kb == pc.kb && kk == 0) ? 0u : 1u;
-            tc::mma_tf32(d, a_hi, b_hi, IDESC, first);
-            tc::mma_tf32(d, a_hi, b_lo, IDESC, 1u);
-            tc::mma_tf32(d, a_lo, b_hi, IDESC, 1u);
+            if (TWO_SM) {
+              tc::mma_tf32_pair(d, a_hi, b_hi, IDESC_PAIR, first);
+              tc::mma_tf32_pair(d, a_hi, b_lo, IDESC_PAIR, 1u);
+              tc::mma_tf32_pair(d, a_lo, b_hi, IDESC_PAIR, 1u);
+            } else {
+              tc::mma_tf32(d, a_hi, b_hi, IDESC, first);
+              tc::mma_tf32(d, a_hi, b_lo, IDESC, 1u);
+              tc::mma_tf32(d, a_lo, b_hi, IDESC, 1u);
+            }
           }
           issued_any = true;
           // frees the stage (in both CTAs of a pair) once these MMAs are done
-          if (CL == 1)
+          if (TWO_SM)
+            tc::commit_pair_multicast(ptx::smem_addr(&bar->empty[s]), kPair);
+          else if (CL == 1)
             tc::commit(ptx::smem_addr(&bar->empty[s]));
           else
             tc::commit_multicast(ptx::smem_addr(&bar->empty[s]), kPair);
         }
         if (!ok) break;
-        tc::commit(ptx::smem_addr(&bar->tmem_full[buf]));  // the piece's accumulator is ready
+        // the piece's accumulator is ready (in both CTAs, in the two-SM form)
+        if (TWO_SM)
+          tc::commit_pair_multicast(ptx::smem_addr(&bar->tmem_full[buf]), kPair);
+        else
+          tc::commit(ptx::smem_addr(&bar->tmem_full[buf]));
       }
       if (*abort_w && issued_any) {
         // wait (bounded) until every MMA issued has completed
-        tc::commit(ptx::smem_addr(&bar->drain));
+        if (TWO_SM)
+          tc::commit_pair(ptx::smem_addr(&bar->drain));
+        else
+          tc::commit(ptx::smem_addr(&bar->drain));
         const uint64_t t0 = ptx::global_ns();
         while (!ptx::mbar_try_wait(ptx::smem_addr(&bar->drain), 0u))
           if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
@@ -378,7 +468,9 @@ __global__ void __launch_bounds__(NT, 1)
         // the MMAs read these tiles through the async proxy
         ptx::fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bar->conv[s]));
+        if (lane == 0) {
+          ptx::mbar_arrive(ptx::smem_addr(&bar->conv[s]));
+        }
       }
     }
   } else {
@@ -397,9 +489,9 @@ __global__ void __launch_bounds__(NT, 1)
     };
     for (int i = 0; i < npieces && !*abort_w; ++i) {
       const Piece pc = get_piece(sc, b, i);
-      const int buf = i & 1;
+      const int buf = i % NBUF;
       const uint32_t acc = tmem + (uint32_t)(buf * ACC_COLS) + lane_base;
-      const bool ok = bounded_wait(ptx::smem_addr(&bar->tmem_full[buf]), (uint32_t)((i >> 1) & 1),
+      const bool ok = bounded_wait(ptx::smem_addr(&bar->tmem_full[buf]), (uint32_t)((i / NBUF) & 1),
                                    abort_w, p.status, kDevTimeoutFull, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after_sync();
@@ -519,18 +611,34 @@ __global__ void __launch_bounds__(NT, 1)
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bar->tmem_empty[buf]));
+      if (lane == 0) {
+        // the even CTA's MMA thread waits for both CTAs' epilogues
+        if (TWO_SM && rank != 0)
+          ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_addr(&bar->tmem_empty[buf]), 0u));
+        else
+          ptx::mbar_arrive(ptx::smem_addr(&bar->tmem_empty[buf]));
+      }
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, TMEM_COLS);
+  if (TWO_SM) {
+    // the even CTA's MMAs write the odd CTA's TMEM and read its shared
+    // memory: the pair frees its TMEM together, once both are done
+    ptx::cluster_sync();
+    if (warp == 1) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc<CG>(tmem, TMEM_COLS);
+    }
+  } else {
+    if (warp == 1) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+    // neither CTA of a pair leaves while the other may still write to it
+    if (CL == 2) ptx::cluster_sync();
   }
-  // neither CTA of a pair leaves while the other may still write to it
-  if (CL == 2) ptx::cluster_sync();
 }
 
 // Per-device set-up (shared-memory attributes, how many CTA pairs can be
@@ -538,7 +646,8 @@ __global__ void __launch_bounds__(NT, 1)
 std::mutex g_mutex;
 bool g_ready[64];
 int g_pairs[64];          // resident clusters of two; 0 = the pair form cannot run
-std::atomic<int> g_cluster_size{2};  // 2: the pair form where possible; 1: single CTAs
+// the requested Form; the pair forms run where possible
+std::atomic<int> g_form{kTwoSmPair};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_tried = false;
 
@@ -608,10 +717,13 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     if (dev < 0 || dev >= 64) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     if (!x3::g_ready[dev]) {
       const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-      if (cudaFuncSetAttribute(x3::gemm_kernel<1, 16>, attr, x3::SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(x3::gemm_kernel<2, 16>, attr, x3::SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(x3::gemm_kernel<1, 32>, attr, x3::SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(x3::gemm_kernel<2, 32>, attr, x3::SMEM_BYTES) != cudaSuccess) {
+      using namespace x3;
+      if (cudaFuncSetAttribute(gemm_kernel<kSingle, 16>, attr, SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kSingle, 32>, attr, SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kMulticastPair, 16>, attr, SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kMulticastPair, 32>, attr, SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kTwoSmPair, 16>, attr, SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kTwoSmPair, 32>, attr, SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
       }
@@ -628,19 +740,26 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
       qc.dynamicSmemBytes = x3::SMEM_BYTES;
       qc.attrs = qa;
       qc.numAttrs = 1;
-      // both widths have the same block and shared-memory size; take the smaller
-      int n16 = 0, n32 = 0;
-      if (cudaOccupancyMaxActiveClusters(&n16, x3::gemm_kernel<2, 16>, &qc) != cudaSuccess ||
-          cudaOccupancyMaxActiveClusters(&n32, x3::gemm_kernel<2, 32>, &qc) != cudaSuccess) {
+      // every pair kernel has the same block and shared-memory size; take the smallest
+      int n[4] = {0, 0, 0, 0};
+      if (cudaOccupancyMaxActiveClusters(&n[0], gemm_kernel<kMulticastPair, 16>, &qc) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveClusters(&n[1], gemm_kernel<kMulticastPair, 32>, &qc) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveClusters(&n[2], gemm_kernel<kTwoSmPair, 16>, &qc) != cudaSuccess ||
+          cudaOccupancyMaxActiveClusters(&n[3], gemm_kernel<kTwoSmPair, 32>, &qc) != cudaSuccess) {
         cudaGetLastError();
-        n16 = n32 = 0;
+        n[0] = 0;
       }
-      x3::g_pairs[dev] = n16 < n32 ? n16 : n32;
+      int least = n[0];
+      for (int j = 1; j < 4; ++j) least = n[j] < least ? n[j] : least;
+      x3::g_pairs[dev] = least;
       x3::g_ready[dev] = true;
     }
     pairs = x3::g_pairs[dev];
   }
-  int CL = (x3::g_cluster_size.load() == 2 && pairs > 0) ? 2 : 1;
+  const int want = x3::g_form.load();
+  int form = (want != x3::kSingle && pairs > 0) ? want : (int)x3::kSingle;
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   {
     std::lock_guard<std::mutex> lock(x3::g_mutex);
@@ -652,16 +771,26 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   // the pair form a schedule unit is two vertically adjacent tiles (a tile row
   // pair), handed to one cluster.
   const int tiles_m = (M + x3::BM - 1) / x3::BM, tiles_n = (N + x3::BN - 1) / x3::BN;
-  const int bk = K >= 1024 ? 16 : 32;  // the k-slice width (see Slice)
-  const int kiters = (K + bk - 1) / bk;
-  const int min_units = 64 / bk;  // at least 64 of K per CTA in a split
-  Schedule sched = make_schedule((tiles_m + 1) / 2, tiles_n, kiters, pairs, 4, min_units);
-  if (CL == 2 && sched.dp_tiles == 0) {
-    // every tile is split along K: the pairs' lockstep costs more than the
-    // shared B tiles save (measured at 1024^3, 2048^3 and 16384 x 64 x 4096)
-    CL = 1;
+  // the k-slice width (see Slice). The two-SM form always takes 32: its
+  // stages halve the per-stage hand-offs between the CTAs of a pair
+  // (measured at 4096^3: 265 against 158 TFLOP/s with 16).
+  auto slice_width = [K](int f) { return (f == x3::kTwoSmPair || K < 1024) ? 32 : 16; };
+  int bk = slice_width(form);
+  int kiters = (K + bk - 1) / bk;
+  Schedule sched{};
+  if (form != x3::kSingle) {
+    sched = make_schedule((tiles_m + 1) / 2, tiles_n, kiters, pairs, 4, 64 / bk);
+    // every tile split along K: the pairs' lockstep costs more than they save
+    // (measured at 1024^3, 2048^3 and 16384 x 64 x 4096)
+    if (sched.dp_tiles == 0) form = x3::kSingle;
   }
-  if (CL == 1) sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, min_units);
+  if (form == x3::kSingle) {
+    bk = slice_width(form);
+    kiters = (K + bk - 1) / bk;
+    // at least 64 of K per CTA in a split
+    sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, 64 / bk);
+  }
+  const int CL = form == x3::kSingle ? 1 : 2;
   const bool split = sched.dp_tiles < sched.tiles;
   const int ctas = sched.grid * CL;
 
@@ -717,9 +846,9 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   p.timeout_ns = library_wait_timeout_ns();
   if (CL == 1) {
     if (bk == 16)
-      x3::gemm_kernel<1, 16><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
+      x3::gemm_kernel<x3::kSingle, 16><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
     else
-      x3::gemm_kernel<1, 32><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
+      x3::gemm_kernel<x3::kSingle, 32><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
   } else {
     cudaLaunchConfig_t lc = {};
@@ -734,9 +863,14 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     lc.stream = stream;
     lc.attrs = la;
     lc.numAttrs = 1;
-    const cudaError_t e =
-        bk == 16 ? cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 16>, p, mA, mB)
-                 : cudaLaunchKernelEx(&lc, x3::gemm_kernel<2, 32>, p, mA, mB);
+    using namespace x3;
+    cudaError_t e;
+    if (form == kTwoSmPair)
+      e = bk == 16 ? cudaLaunchKernelEx(&lc, gemm_kernel<kTwoSmPair, 16>, p, mA, mB)
+                   : cudaLaunchKernelEx(&lc, gemm_kernel<kTwoSmPair, 32>, p, mA, mB);
+    else
+      e = bk == 16 ? cudaLaunchKernelEx(&lc, gemm_kernel<kMulticastPair, 16>, p, mA, mB)
+                   : cudaLaunchKernelEx(&lc, gemm_kernel<kMulticastPair, 32>, p, mA, mB);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return SGEMM_ERR_LAUNCH;
@@ -744,14 +878,17 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   }
   char text[160];
   snprintf(text, sizeof(text),
-           "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d grid=%d units=%d dp=%d split=%d kiters=%d%s",
-           x3::BM, x3::BN, bk, 64 / bk, CL, ctas, sched.grid, sched.dp_tiles,
+           "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d%s grid=%d units=%d dp=%d split=%d kiters=%d%s",
+           x3::BM, x3::BN, bk, (form == x3::kTwoSmPair ? 96 : 64) / bk, CL,
+           form == x3::kTwoSmPair ? " pair=2sm" : (form == x3::kMulticastPair ? " pair=multicast" : ""),
+           ctas, sched.grid, sched.dp_tiles,
            sched.tiles - sched.dp_tiles, kiters, a_direct ? "" : " a=copied");
   note_last_config(text);
   return SGEMM_OK;
 }
 
-SGEMM_API int sgemm_3xtf32_set_cluster_size(int cluster_size) {
-  if (cluster_size != 1 && cluster_size != 2) return SGEMM_ERR_INVALID_VALUE;
-  return x3::g_cluster_size.exchange(cluster_size);
+SGEMM_API int sgemm_3xtf32_set_kernel_form(int form) {
+  if (form != SGEMM_X3_SINGLE && form != SGEMM_X3_PAIR && form != SGEMM_X3_PAIR_MULTICAST)
+    return SGEMM_ERR_INVALID_VALUE;
+  return x3::g_form.exchange(form);
 }

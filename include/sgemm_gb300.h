@@ -103,15 +103,24 @@ int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, cons
                  int ldb, float beta, float* C, int ldc, void* stream);
 
 /*
- * Kernel form of sgemm_3xtf32 for later calls (process-wide): 2 (the default)
- * runs clusters of two CTAs on vertically adjacent tiles that share each B
- * tile through TMA multicast, where the device can co-schedule CTA pairs and
- * the problem has at least two waves of whole tile pairs (else single CTAs);
- * 1 always runs single CTAs, each loading its own B tiles. Both give the
- * same results within the tolerance (bit-identical on integer inputs). Returns the previous setting, or
- * SGEMM_ERR_INVALID_VALUE (nothing changed) for another value.
+ * Kernel form of sgemm_3xtf32 for later calls (process-wide):
+ *   SGEMM_X3_PAIR (the default): clusters of two CTAs on vertically adjacent
+ *     128 x 256 tiles; the even CTA issues M = 256 MMAs over both
+ *     (tcgen05 cta_group::2), each CTA holding its A tile and half of the B
+ *     tile in shared memory and its 128 rows of the accumulator in TMEM;
+ *   SGEMM_X3_PAIR_MULTICAST: clusters of two CTAs on the same tiles that share
+ *     each B tile through TMA multicast, each issuing its own M = 128 MMAs;
+ *   SGEMM_X3_SINGLE: single CTAs, each loading its own B tiles.
+ * The pair forms run where the device can co-schedule CTA pairs and the
+ * problem has at least two waves of whole tile pairs, else single CTAs. All
+ * give the same results within the tolerance (bit-identical on integer
+ * inputs). Returns the previous setting, or SGEMM_ERR_INVALID_VALUE (nothing
+ * changed) for another value.
  */
-int sgemm_3xtf32_set_cluster_size(int cluster_size);
+#define SGEMM_X3_SINGLE 1
+#define SGEMM_X3_PAIR 2
+#define SGEMM_X3_PAIR_MULTICAST 3
+int sgemm_3xtf32_set_kernel_form(int form);
 
 /*
  * C = alpha * op(A) * op(B) + beta * C, row-major, FFMA path. op(A) is M x K:

@@ -60,16 +60,16 @@ def test_sgemm_graph_replays(w):
         assert "split=" in cfg and "split=0" not in cfg
 
 
-@pytest.mark.parametrize("cluster", [2, 1])
+@pytest.mark.parametrize("form", binding.X3_FORMS)
 @pytest.mark.parametrize("w", [Workload("x3graph", 300, 700, 3000, 1.25, -0.5, "int3", 93),
                                Workload("x3graphpairs", 128 * 2 * 76 * 2, 256, 64, 1.0, 1.0,
                                         "int3", 94)], ids=lambda w: w.name)
-def test_3xtf32_graph_replays(w, cluster):
-    prev = binding.sgemm_3xtf32_set_cluster_size(cluster)
+def test_3xtf32_graph_replays(w, form):
+    prev = binding.sgemm_3xtf32_set_kernel_form(form)
     try:
         _replay_and_check(binding.sgemm_3xtf32, w, replays=2)
     finally:
-        binding.sgemm_3xtf32_set_cluster_size(prev)
+        binding.sgemm_3xtf32_set_kernel_form(prev)
 
 
 def test_batched_graph_replays():

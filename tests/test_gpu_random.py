@@ -1,7 +1,7 @@
 """Seeded random cases against the oracle: shapes, padded leading dimensions,
 pointer offsets, alpha and beta (zero included), input distributions,
 operand forms, batch counts, forced tile configurations, and each entry point
-(sgemm, sgemm_ex, sgemm_strided_batched, sgemm_3xtf32 in both kernel forms,
+(sgemm, sgemm_ex, sgemm_strided_batched, sgemm_3xtf32 in its three kernel forms,
 sgemm_ladder, sgemm_noalloc, and sgemm_host on pinned or pageable host
 memory). Every case is a fixed function of its index, so a failure
 names a reproducible case. Padding holds NaN: a read outside an operand
@@ -43,7 +43,7 @@ def _case(i):
         opB=int(r.integers(0, 2)) if entry in ("sgemm_ex", "batched") else N_,
         batch=int(r.integers(1, 4)) if entry == "batched" else 1,
         config=int(r.integers(-1, compiled_config_count())),
-        cluster=int(r.integers(1, 3)),
+        x3form=int(r.integers(1, 4)),
         kernel=int(r.choice(binding.LADDER_KERNELS)),
         seed=int(r.integers(0, 2**31 - 1)),
         pinned=bool(r.integers(0, 2)),
@@ -112,7 +112,7 @@ def test_random_case(i):
     alpha, beta = c["alpha"], c["beta"]
     if e in ("sgemm", "sgemm_ex", "batched"):
         assert binding.sgemm_force_config(c["config"]) == 0
-    prev_cluster = binding.sgemm_3xtf32_set_cluster_size(c["cluster"])
+    prev_form = binding.sgemm_3xtf32_set_kernel_form(c["x3form"])
     try:
         if e == "sgemm":
             st = binding.sgemm(M, N, K, alpha, pA, lda, pB, ldb, beta, pC, ldc, s)
@@ -137,7 +137,7 @@ def test_random_case(i):
             assert binding.sgemm_poll_device_status(s) == (0, 0)
     finally:
         binding.sgemm_force_config(-1)
-        binding.sgemm_3xtf32_set_cluster_size(prev_cluster)
+        binding.sgemm_3xtf32_set_kernel_form(prev_form)
     if e != "host":
         H.assert_guards_intact(storeC, c["offsets"][2], dC.numel(), what=f"case {c}")
     out = dC.cpu().numpy() if e != "host" else dC.numpy()

@@ -2,8 +2,8 @@
 bar as the FFMA path -- bit-exact on integer inputs, the FP32 tolerance
 |C - C_ref| <= 1e-5 * (|alpha| sum |a||b| + |beta| |c|) + 1e-30 on real inputs --
 on small shapes element by element and on the full workloads by sampling.
-Every test runs in both kernel forms: CTA pairs sharing B tiles by multicast
-(the default) and single CTAs."""
+Every test runs in the three kernel forms: CTA pairs with two-SM MMAs (the
+default), CTA pairs sharing B tiles by multicast, and single CTAs."""
 import numpy as np
 import pytest
 import torch
@@ -17,21 +17,26 @@ pytestmark = pytest.mark.gpu
 X3 = binding.sgemm_3xtf32
 
 
-@pytest.fixture(autouse=True, params=[2, 1], ids=["pairs", "single"])
-def cluster_size(request):
-    prev = binding.sgemm_3xtf32_set_cluster_size(request.param)
+FORM_TEXT = {binding.SGEMM_X3_PAIR: "cluster=2 pair=2sm",
+             binding.SGEMM_X3_PAIR_MULTICAST: "cluster=2 pair=multicast",
+             binding.SGEMM_X3_SINGLE: "cluster=1 "}
+
+
+@pytest.fixture(autouse=True, params=binding.X3_FORMS, ids=["pair2sm", "multicast", "single"])
+def kernel_form(request):
+    prev = binding.sgemm_3xtf32_set_kernel_form(request.param)
     yield request.param
-    binding.sgemm_3xtf32_set_cluster_size(prev)
+    binding.sgemm_3xtf32_set_kernel_form(prev)
 
 
-def test_kernel_form_is_reported(cluster_size):
-    # two waves of whole tile pairs: the pair form runs when selected
+def test_kernel_form_is_reported(kernel_form):
+    # two waves of whole tile pairs: the pair forms run when selected
     w = Workload("x3form", 128 * 2 * 76 * 2, 256, 64, 1.0, 0.0, "int3", 36)
     H.check_sampled(w, rows=64, elements=4096, fn=X3)
-    assert f"cluster={cluster_size}" in binding.sgemm_last_config()
+    assert FORM_TEXT[kernel_form] in binding.sgemm_last_config()
     # every tile split along K: single CTAs either way
     H.check_against_oracle(Workload("x3split", 300, 520, 4000, 1.0, 0.0, "int3", 37), fn=X3)
-    assert "cluster=1" in binding.sgemm_last_config()
+    assert "cluster=1 " in binding.sgemm_last_config()
 
 SHAPES = [(128, 256, 32), (1, 1, 1), (7, 9, 3), (33, 65, 17), (257, 129, 100), (300, 520, 77),
           (129, 257, 1000), (513, 1031, 40), (64, 64, 4097), (2, 700, 2049), (1000, 40, 129)]
@@ -93,9 +98,16 @@ def test_sweep_integer_bit_exact(n):
     H.check_sampled(WORKLOADS[f"sweep{n}_int"], rows=4, elements=512, fn=X3)
 
 
-def test_slice_width_follows_k():
-    # BK = 32 (two stages) below K = 1024, BK = 16 (four stages) from there
+def test_slice_width_follows_k(kernel_form):
+    # single CTAs: BK = 32 (two stages) below K = 1024, BK = 16 (four stages) from there
     H.check_against_oracle(Workload("x3k", 200, 300, 1023, 1.0, 0.5, "int3", 38), fn=X3)
     assert "128x256x32_s2" in binding.sgemm_last_config()
     H.check_against_oracle(Workload("x3k", 200, 300, 1024, 1.0, 0.5, "int3", 38), fn=X3)
     assert "128x256x16_s4" in binding.sgemm_last_config()
+    # whole waves of tile pairs at K = 1024: the two-SM form keeps BK = 32
+    # (three stages of half B tiles), the multicast form takes BK = 16
+    H.check_sampled(Workload("x3k2", 128 * 2 * 76 * 2, 256, 1024, 1.0, 0.5, "int3", 39),
+                    rows=32, elements=2048, fn=X3)
+    want = {binding.SGEMM_X3_PAIR: "128x256x32_s3", binding.SGEMM_X3_PAIR_MULTICAST: "128x256x16_s4",
+            binding.SGEMM_X3_SINGLE: "128x256x16_s4"}[kernel_form]
+    assert want in binding.sgemm_last_config()
