@@ -29,16 +29,24 @@
 //      three tcgen05.mma.kind::tf32 products; warps 2-5 read an accumulator
 //      back with tcgen05.ld and apply alpha * acc + beta * C.
 //
-// Cluster form (CL = 2, the default where the device can co-schedule CTA
-// pairs): the two CTAs of a cluster compute vertically adjacent tiles (tile
-// rows 2i and 2i + 1 of the same tile column) in lockstep, so they need the
-// same B tile. Each CTA loads its own A tiles and one half (128 rows) of the
-// B_hi and B_lo tiles, multicast into both CTAs' shared memory: the pair
-// reads B from L2 once instead of twice, a third less operand traffic per
-// CTA. A stage is refilled only after the MMAs of both CTAs have read it
-// (each MMA warp's commit arrives on the "empty" barrier of both CTAs), and
-// before exiting every CTA waits until its barriers have received the peer's
-// last arrivals, then meets the peer at a cluster barrier.
+// Kernel forms (sgemm_3xtf32_set_kernel_form):
+//   * two-SM pairs (the default where the device co-schedules CTA pairs and
+//     the problem has two waves of whole tile pairs): the CTAs of a cluster
+//     of two take tile rows 2i and 2i + 1 of one tile column. Each holds its
+//     A tile and one half (128 columns) of the B tile, so a 32-wide stage is
+//     64 KB; the even CTA issues M = 256 MMAs (cta_group::2) that read A and
+//     B from both CTAs' shared memory and write each CTA's 128 accumulator
+//     rows into its own TMEM. The even CTA's conv barrier completes when the
+//     converters of both CTAs are done (the odd CTA's through one relayed
+//     remote arrival per stage); its commits free the stage and publish the
+//     accumulator in both CTAs; its MMA thread waits for both epilogues.
+//   * multicast pairs: the same tile pairs, each CTA loading its A tile and
+//     one half of the B tile into both CTAs by TMA multicast and issuing its
+//     own M = 128 MMAs; a stage is refilled once both CTAs' MMAs read it.
+//   * single CTAs, each with its own A and B tiles.
+// Before exiting, a CTA of a pair waits (bounded) until its barriers have
+// received the peer's last arrivals, then meets the peer at a cluster
+// barrier (two-SM pairs free their TMEM together after it).
 // Every wait is bounded (see ffma_sgemm.cuh); a CTA that gives up drains its
 // copies and MMAs, frees its TMEM and returns.
 #include <cuda.h>
