@@ -110,6 +110,14 @@ constexpr int kernel_smem_bytes() {
   return smem_bytes(S);
 }
 
+// Bound of the clean-up waits of an aborting CTA (copies and MMAs it already
+// issued, a peer's last arrivals): these end within microseconds, so the bound
+// is at least 100 ms whatever the detection timeout, and a short timeout never
+// lets a CTA free its tensor memory or exit with work still in flight.
+__device__ __forceinline__ long long cleanup_bound_ns(long long timeout_ns) {
+  return timeout_ns > 100000000LL ? timeout_ns : 100000000LL;
+}
+
 // Bounded wait on an mbarrier phase. Returns false (after recording `code`
 // and raising the CTA's abort word) if the phase does not complete within
 // timeout_ns, or if another thread has already raised the abort word.
@@ -694,7 +702,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
         const uint32_t fb = ptx::smem_addr(&bb->fullB[s % ST]);
         const uint32_t par = (uint32_t)((s / ST) & 1);
         while (!ptx::mbar_try_wait(fb, par)) {
-          if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+          if ((long long)(ptx::global_ns() - t0) > cleanup_bound_ns(p.timeout_ns)) break;
         }
       }
     }

@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(NT, 1)
       for (int j = it - 1; j >= 0 && j >= it - ST; --j) {
         const uint32_t fb = ptx::smem_addr(&bar->full[j % ST]);
         while (!ptx::mbar_try_wait(fb, (uint32_t)((j / ST) & 1)))
-          if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+          if ((long long)(ptx::global_ns() - t0) > cleanup_bound_ns(p.timeout_ns)) break;
       }
       if (CL == 2) {
         // the peer's MMA warp (the even CTA's, in the two-SM form) arrives on
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int j = it; j < it + ST; ++j) {
           const uint32_t eb = ptx::smem_addr(&bar->empty[j % ST]);
           while (!ptx::mbar_try_wait(eb, (uint32_t)((j / ST) & 1) ^ 1u))
-            if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+            if ((long long)(ptx::global_ns() - t0) > cleanup_bound_ns(p.timeout_ns)) break;
         }
       }
     }
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(NT, 1)
           tc::commit(ptx::smem_addr(&bar->drain));
         const uint64_t t0 = ptx::global_ns();
         while (!ptx::mbar_try_wait(ptx::smem_addr(&bar->drain), 0u))
-          if ((long long)(ptx::global_ns() - t0) > p.timeout_ns) break;
+          if ((long long)(ptx::global_ns() - t0) > cleanup_bound_ns(p.timeout_ns)) break;
       }
     }
   } else if (warp >= CONV_WARP0) {
