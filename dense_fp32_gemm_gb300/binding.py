@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_host": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_ladder": (I, [I, I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_3xtf32_set_kernel_form": (I, [I]),
+                "sgemm_3xtf32_plan": (I, [I, I, I, I, I, I, IP]),
                 "sgemm_host_set_pipeline": (I, [I, I, I, I]),
                 "sgemm_config_layouts": (I, [I]),
                 "sgemm_diag_tf32_mma_rate": (I, [I, ctypes.POINTER(ctypes.c_double)]),
@@ -262,6 +263,16 @@ LADDER_KERNELS = (3, 7, 8)
 
 SGEMM_X3_SINGLE, SGEMM_X3_PAIR, SGEMM_X3_PAIR_MULTICAST = 1, 2, 3
 X3_FORMS = (SGEMM_X3_PAIR, SGEMM_X3_PAIR_MULTICAST, SGEMM_X3_SINGLE)
+
+
+X3_PLAN_FIELDS = ("form", "bk", "stages", "ctas", "units", "dp_units", "split_units", "kiters")
+
+
+def sgemm_3xtf32_plan(M: int, N: int, K: int, form: int, pairs: int, sms: int):
+    """(status, {field: value}) of the plan sgemm_3xtf32 follows (host only)."""
+    out = _ints(len(X3_PLAN_FIELDS))
+    st = lib().sgemm_3xtf32_plan(M, N, K, form, pairs, sms, out)
+    return st, dict(zip(X3_PLAN_FIELDS, list(out)))
 
 
 def sgemm_3xtf32_set_kernel_form(form: int) -> int:

@@ -659,6 +659,42 @@ std::atomic<int> g_form{kTwoSmPair};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_tried = false;
 
+// The launch plan of sgemm_3xtf32 (host arithmetic only): the kernel form
+// that runs, the k-slice width and the persistent schedule. `want` is the
+// requested form, `pairs` how many CTA pairs the device keeps resident (0:
+// none), `sms` the SM count.
+struct Plan {
+  int form, bk, kiters;
+  Schedule sched;
+};
+Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
+  Plan pl{};
+  pl.form = (want != kSingle && pairs > 0) ? want : (int)kSingle;
+  // schedule: whole tiles, then the last one to two waves split along K. In
+  // the pair forms a schedule unit is two vertically adjacent tiles (a tile
+  // row pair), handed to one cluster.
+  const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+  // the k-slice width (see Slice). The two-SM form always takes 32: its
+  // stages halve the per-stage hand-offs between the CTAs of a pair
+  // (measured at 4096^3: 265 against 158 TFLOP/s with 16).
+  auto slice_width = [K](int f) { return (f == kTwoSmPair || K < 1024) ? 32 : 16; };
+  pl.bk = slice_width(pl.form);
+  pl.kiters = (K + pl.bk - 1) / pl.bk;
+  if (pl.form != kSingle) {
+    pl.sched = make_schedule((tiles_m + 1) / 2, tiles_n, pl.kiters, pairs, 4, 64 / pl.bk);
+    // every tile split along K: the pairs' lockstep costs more than they save
+    // (measured at 1024^3, 2048^3 and 16384 x 64 x 4096)
+    if (pl.sched.dp_tiles == 0) pl.form = kSingle;
+  }
+  if (pl.form == kSingle) {
+    pl.bk = slice_width(pl.form);
+    pl.kiters = (K + pl.bk - 1) / pl.bk;
+    // at least 64 of K per CTA in a split
+    pl.sched = make_schedule(tiles_m, tiles_n, pl.kiters, sms, 8, 64 / pl.bk);
+  }
+  return pl;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   if (!g_encode_tried) {
     g_encode_tried = true;
@@ -766,8 +802,6 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     }
     pairs = x3::g_pairs[dev];
   }
-  const int want = x3::g_form.load();
-  int form = (want != x3::kSingle && pairs > 0) ? want : (int)x3::kSingle;
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   {
     std::lock_guard<std::mutex> lock(x3::g_mutex);
@@ -775,29 +809,9 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   }
   if (enc == nullptr) return SGEMM_ERR_LAUNCH;
 
-  // schedule: whole tiles, then the last one to two waves split along K. In
-  // the pair form a schedule unit is two vertically adjacent tiles (a tile row
-  // pair), handed to one cluster.
-  const int tiles_m = (M + x3::BM - 1) / x3::BM, tiles_n = (N + x3::BN - 1) / x3::BN;
-  // the k-slice width (see Slice). The two-SM form always takes 32: its
-  // stages halve the per-stage hand-offs between the CTAs of a pair
-  // (measured at 4096^3: 265 against 158 TFLOP/s with 16).
-  auto slice_width = [K](int f) { return (f == x3::kTwoSmPair || K < 1024) ? 32 : 16; };
-  int bk = slice_width(form);
-  int kiters = (K + bk - 1) / bk;
-  Schedule sched{};
-  if (form != x3::kSingle) {
-    sched = make_schedule((tiles_m + 1) / 2, tiles_n, kiters, pairs, 4, 64 / bk);
-    // every tile split along K: the pairs' lockstep costs more than they save
-    // (measured at 1024^3, 2048^3 and 16384 x 64 x 4096)
-    if (sched.dp_tiles == 0) form = x3::kSingle;
-  }
-  if (form == x3::kSingle) {
-    bk = slice_width(form);
-    kiters = (K + bk - 1) / bk;
-    // at least 64 of K per CTA in a split
-    sched = make_schedule(tiles_m, tiles_n, kiters, sms, 8, 64 / bk);
-  }
+  const x3::Plan plan = x3::make_plan(M, N, K, x3::g_form.load(), pairs, sms);
+  const int form = plan.form, bk = plan.bk, kiters = plan.kiters;
+  const Schedule& sched = plan.sched;
   const int CL = form == x3::kSingle ? 1 : 2;
   const bool split = sched.dp_tiles < sched.tiles;
   const int ctas = sched.grid * CL;
@@ -892,6 +906,23 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
            ctas, sched.grid, sched.dp_tiles,
            sched.tiles - sched.dp_tiles, kiters, a_direct ? "" : " a=copied");
   note_last_config(text);
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sms, int* out) {
+  if (M < 1 || N < 1 || K < 1) return SGEMM_ERR_INVALID_DIM;
+  if ((form != SGEMM_X3_SINGLE && form != SGEMM_X3_PAIR && form != SGEMM_X3_PAIR_MULTICAST) ||
+      pairs < 0 || sms < 1 || out == nullptr)
+    return SGEMM_ERR_INVALID_VALUE;
+  const x3::Plan pl = x3::make_plan(M, N, K, form, pairs, sms);
+  out[0] = pl.form;
+  out[1] = pl.bk;
+  out[2] = (pl.form == x3::kTwoSmPair ? 96 : 64) / pl.bk;   // stages
+  out[3] = pl.sched.grid * (pl.form == x3::kSingle ? 1 : 2);  // CTAs
+  out[4] = pl.sched.grid;                                    // schedule units
+  out[5] = pl.sched.dp_tiles;
+  out[6] = pl.sched.tiles - pl.sched.dp_tiles;
+  out[7] = pl.kiters;
   return SGEMM_OK;
 }
 

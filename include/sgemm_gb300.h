@@ -123,6 +123,19 @@ int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, cons
 int sgemm_3xtf32_set_kernel_form(int form);
 
 /*
+ * The plan sgemm_3xtf32 follows for an M x N x K problem (host arithmetic
+ * only, no device needed): `form` is the requested kernel form, `pairs` how
+ * many CTA pairs the device keeps resident (0: none), `sms` its SM count.
+ * out = {form that runs, k-slice width, stages, CTAs, schedule units (a CTA
+ * pair each in the pair forms), whole-tile units, K-split units, k-slices}.
+ * The pair forms fall back to single CTAs when pairs == 0 or when every tile
+ * would be split along K. Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM unless
+ * M, N, K >= 1 (only such problems launch the GEMM kernel), or
+ * SGEMM_ERR_INVALID_VALUE for another form, pairs < 0, sms < 1 or a NULL out.
+ */
+int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sms, int* out);
+
+/*
  * C = alpha * op(A) * op(B) + beta * C, row-major, FFMA path. op(A) is M x K:
  * A itself (SGEMM_OP_N, stored M x K, lda >= max(1, K)) or the transpose of an
  * A stored K x M (SGEMM_OP_T, lda >= max(1, M)); op(B) is K x N: B (stored
