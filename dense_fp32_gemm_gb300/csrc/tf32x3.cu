@@ -80,13 +80,18 @@ namespace x3 {
 
 constexpr int BM = 128, BN = 256, NT = 320;
 
+constexpr int kStageRegion = 192 * 1024;  // the ring of stages
+constexpr int kMaxStages = 6;
+
 // The k-slice: BK values of K per stage, in swizzled rows of 4 * BK bytes,
-// with as many stages as fit in 192 KB. BK = 16 (four 48 KB stages, 64-byte
-// swizzle) lets the loads run three stages ahead of the MMAs; BK = 32 (two
-// 96 KB stages, 128-byte swizzle) has half the per-stage hand-offs. Measured
-// on GB300: 16 is faster from K = 1024 up (4096^3: 251 against 226 TFLOP/s),
-// 32 below (8191 x 1000 x 777: 99 against 86 TFLOP/s).
-// B_PARTS = 2 (the two-SM form): a CTA holds half of each B tile.
+// with as many stages as fit in the stage region. With whole B tiles, BK = 16
+// (four 48 KB stages, 64-byte swizzle) lets the loads run three stages ahead
+// of the MMAs and BK = 32 (two 96 KB stages, 128-byte swizzle) has half the
+// per-stage hand-offs; measured on GB300, 16 is faster from K = 1024 up
+// (4096^3: 251 against 226 TFLOP/s), 32 below (8191 x 1000 x 777: 99 against
+// 86 TFLOP/s). B_PARTS = 2 (the two-SM form): a CTA holds half of each B
+// tile, and BK = 32 gives three 64 KB stages (its hand-offs between the CTAs
+// of a pair cost more, so it always takes 32).
 template <int BK_, int B_PARTS = 1>
 struct Slice {
   static constexpr int BK = BK_;
@@ -97,10 +102,8 @@ struct Slice {
   // a stage: [A_hi | A_lo | B_hi | B_lo]; TMA writes the _hi tiles (the raw
   // values), the converter warps the _lo tiles
   static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 / 48 KB, or 64 / 32 KB
-  static constexpr int ST = 192 * 1024 / STAGE_BYTES;              // 2 / 4, or 3 / 6
+  static constexpr int ST = kStageRegion / STAGE_BYTES;            // 2 / 4, or 3 / 6
 };
-constexpr int kMaxStages = 6;
-constexpr int kStageRegion = 192 * 1024;
 static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
                   Slice<32>::ST * Slice<32>::STAGE_BYTES == kStageRegion &&
                   Slice<16, 2>::ST * Slice<16, 2>::STAGE_BYTES == kStageRegion &&
@@ -125,9 +128,11 @@ static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
 struct Barriers {
   uint64_t full[kMaxStages];   // TMA transaction bytes of one stage (the raw tiles)
   uint64_t conv[kMaxStages];   // the converter warps have written the stage's residuals
+                               // (two-SM form, even CTA: also the odd CTA's, relayed)
   uint64_t empty[kMaxStages];  // MMAs that read a stage have completed
-  uint64_t tmem_full[2];   // a piece's last MMA into accumulator i has completed
-  uint64_t tmem_empty[2];  // the epilogue warps have read accumulator i
+  uint64_t tmem_full[NBUF];    // a piece's last MMA into accumulator i has completed
+  uint64_t tmem_empty[NBUF];   // the epilogue warps have read accumulator i (two-SM
+                               // form, even CTA: those of both CTAs)
   uint64_t drain;          // final MMA completion on the abort path
   uint64_t epi_sync;       // rendezvous of the 128 epilogue threads
   uint32_t tmem_addr;
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(NT, 1)
                      CONV_THREADS / 32 + ((TWO_SM && rank == 0) ? 1 : 0));
       ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), TWO_SM ? 1 : CL);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NBUF; ++i) {
       ptx::mbar_init(ptx::smem_addr(&bar->tmem_full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&bar->tmem_empty[i]), (TWO_SM ? 2 : 1) * 4);
     }
@@ -683,7 +688,8 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   if (pl.form != kSingle) {
     pl.sched = make_schedule((tiles_m + 1) / 2, tiles_n, pl.kiters, pairs, 4, 64 / pl.bk);
     // every tile split along K: the pairs' lockstep costs more than they save
-    // (measured at 1024^3, 2048^3 and 16384 x 64 x 4096)
+    // (measured in both pair forms at 1024^3, 1024 x 1024 x 16384 and
+    // 16384 x 64 x 4096; the two-SM form gained 4 % at 2048^3 only)
     if (pl.sched.dp_tiles == 0) pl.form = kSingle;
   }
   if (pl.form == kSingle) {
