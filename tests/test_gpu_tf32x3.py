@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from dense_fp32_gemm_gb300 import binding
 from dense_fp32_gemm_gb300.workloads import SWEEP_SIZES, WORKLOADS, Workload, integer_variant, make_inputs
 
@@ -111,3 +112,21 @@ def test_slice_width_follows_k(kernel_form):
     want = {binding.SGEMM_X3_PAIR: "128x256x32_s3", binding.SGEMM_X3_PAIR_MULTICAST: "128x256x16_s4",
             binding.SGEMM_X3_SINGLE: "128x256x16_s4"}[kernel_form]
     assert want in binding.sgemm_last_config()
+
+
+@pytest.mark.parametrize("dist", ["int3", "uniform"])
+def test_pair_size_with_ragged_edges(dist, kernel_form):
+    # 305 tile rows (the last pair's odd CTA lies below M), a ragged second tile
+    # column and a ragged last k-slice, with whole waves of tile pairs, so the
+    # pair forms run: Freivalds over every element (integer inputs), sampled
+    # rows, and the last 90 rows (the ragged last tile row) against the oracle
+    w = Workload("x3pairedge", 128 * 304 + 88, 300, 1100, 1.25, -0.5, dist, 41)
+    A, B, C = make_inputs(w)
+    out = H.run_cuda(w, A, B, C, fn=X3)
+    assert FORM_TEXT[kernel_form] in binding.sgemm_last_config()
+    gpu = H.logical(out, w.M, w.N, w.LDC)
+    lo = w.M - 90
+    ref, mag = oracle.sgemm_rows(w.M, w.N, w.K, w.alpha, A.numpy(), w.LDA, B.numpy(), w.LDB, w.beta,
+                                 C.numpy(), w.LDC, lo, w.M)
+    H.assert_match(w, gpu[lo:], ref, mag, what="last rows")
+    H.check_sampled(w, rows=32, elements=2048, fn=X3)
