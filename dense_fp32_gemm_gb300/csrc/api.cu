@@ -57,9 +57,6 @@ struct DeviceInfo {
 };
 std::map<int, DeviceInfo> g_devices;
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-bool g_encode_tried = false;
-
 struct Workspace {
   void* block = nullptr;
   size_t bytes = 0;
@@ -98,16 +95,18 @@ int device_info(int dev, DeviceInfo** out) {
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  if (!g_encode_tried) {
-    g_encode_tried = true;
+  // looked up once; the initialisation of a function-local static is thread-safe
+  static const PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  return g_encode;
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cudaGetLastError();
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
+  return enc;
 }
 
 // Workspace of at least `flags` flags and `partial_floats` floats for this

@@ -84,8 +84,6 @@ struct NoAllocDevice {
 
 std::mutex g_na_mutex;
 NoAllocDevice g_na_devices[kNoAllocMaxDevices];  // fixed storage: no heap use
-PFN_cuTensorMapEncodeTiled_v12000 g_na_encode = nullptr;
-bool g_na_encode_tried = false;
 
 // Same schedule constants as sgemm() and the same automatic tile choice
 // (dispatch.hpp), so both entry points run the same kernel and schedule.
@@ -132,16 +130,18 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 noalloc_encoder() {
-  if (!g_na_encode_tried) {
-    g_na_encode_tried = true;
+  // looked up once; the initialisation of a function-local static is thread-safe
+  static const PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      g_na_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  return g_na_encode;
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cudaGetLastError();
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
+  return enc;
 }
 
 __global__ void noalloc_scale_c_kernel(int M, int N, float beta, float* C, long long ldc) {

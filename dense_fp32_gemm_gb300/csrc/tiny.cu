@@ -11,6 +11,7 @@
 // 128-bit forms are used only where the rows allow them.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 
@@ -104,7 +105,9 @@ __global__ void __launch_bounds__(kThreads) tiny_kernel(int M, int N, int K, flo
   }
 }
 
-bool g_attr_set[64];
+// devices whose kernels have their shared-memory attribute set (setting it
+// twice, from two threads, is harmless)
+std::atomic<bool> g_attr_set[64];
 
 }  // namespace tiny
 
@@ -119,14 +122,14 @@ cudaError_t tiny_launch(int dev, int M, int N, int K, float alpha, const float* 
                         const float* B, long long ldb, float beta, float* C, long long ldc,
                         cudaStream_t stream, char* text, int text_len) {
   using namespace tiny;
-  if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+  if (dev < 0 || dev >= 64 || !g_attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(tiny_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(tiny_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemBytes);
     if (e != cudaSuccess) return e;
-    g_attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) g_attr_set[dev].store(true, std::memory_order_release);
   }
   const int tiles_m = (M + kT - 1) / kT, tiles_n = (N + kT - 1) / kT;
   const int grid = tiles_m * tiles_n;  // at most 2^25 / 32 tiles
