@@ -80,14 +80,17 @@ def tf32x3_peak_tflops(peaks):
     return (float(bf16) * TF32_OVER_BF16 / 3.0) if bf16 else None
 
 
-def tf32x3_roof(binding, peaks):
+def tf32x3_roof(binding, peaks, pair=False):
     """(roof TFLOP/s, basis, measured TF32 TFLOP/s or None): the measured
     tcgen05 kind::tf32 throughput of this device / 3 (the library's probe
-    kernel), else the BF16-derived estimate."""
-    st, tf32 = binding.sgemm_diag_tf32_mma_rate(20000)
+    kernels: cta_group::2 MMAs of CTA pairs when `pair`, the form the timed
+    call ran, else one CTA per SM), else the BF16-derived estimate."""
+    probe = binding.sgemm_diag_tf32_pair_mma_rate if pair else binding.sgemm_diag_tf32_mma_rate
+    st, tf32 = probe(20000)
     if st == 0 and tf32 > 0:
-        return (tf32 / 3.0, "measured tcgen05.mma kind::tf32 throughput (probe kernel, one CTA "
-                            "per SM, burst) / 3 TF32 products per FP32 product", tf32)
+        form = ("two-SM pairs, cta_group::2 M 256" if pair else "one CTA per SM, M 128")
+        return (tf32 / 3.0, f"measured tcgen05.mma kind::tf32 throughput (probe kernel, {form}, "
+                            "burst) / 3 TF32 products per FP32 product", tf32)
     return (tf32x3_peak_tflops(peaks), "measured bf16 peak x 1.1/2.25 (TF32/BF16 nominal) / 3 "
                                        "TF32 products per FP32 product", None)
 
@@ -479,7 +482,8 @@ def run_ours(args, w):
         "clocks": clocks,
     }
     if tf32x3 is not None:
-        p3, basis, tf32_measured = tf32x3_roof(binding, peaks)
+        p3, basis, tf32_measured = tf32x3_roof(binding, peaks,
+                                               pair="pair=2sm" in tf32x3["config"])
         a3 = tf32x3["value"] / 1e3
         est = tf32x3_peak_tflops(peaks)
         tf32x3["roofline"] = {"bound": "tensor", "achieved": round(a3, 3),
@@ -574,7 +578,8 @@ def run_report(args):
     peaks = measured_peaks()
     max_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
     peak_tf = ffma_peak_tflops(props.multi_processor_count, max_mhz)
-    p3, _, _ = tf32x3_roof(binding, peaks)
+    # the 3xTF32 roof of each kernel form: single CTAs, and two-SM pairs
+    roof3 = {False: tf32x3_roof(binding, peaks)[0], True: tf32x3_roof(binding, peaks, pair=True)[0]}
     s = torch.cuda.current_stream().cuda_stream
     flush = _l2_flusher()
     for name in REPORT_WORKLOADS:
@@ -601,6 +606,7 @@ def run_report(args):
             if path == "ffma":
                 line["pct_of_ffma_peak"] = round(100 * tf / peak_tf, 2)
             else:
+                p3 = roof3["pair=2sm" in binding.sgemm_last_config()]
                 line["pct_of_3xtf32_tensor_roof"] = round(100 * tf / p3, 2) if p3 else None
             line.update({"min_bytes": mb, "achieved_min_gbs": round(mb / ms / 1e6, 1),
                          "achieved_min_gbs_l2_flushed":

@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_host_set_pipeline": (I, [I, I, I, I]),
                 "sgemm_config_layouts": (I, [I]),
                 "sgemm_diag_tf32_mma_rate": (I, [I, ctypes.POINTER(ctypes.c_double)]),
+                "sgemm_diag_tf32_pair_mma_rate": (I, [I, ctypes.POINTER(ctypes.c_double)]),
                 "sgemm_strided_batched": (I, [I, I, I, I, I, F, P, I, LL, P, I, LL, F, P, I, LL,
                                               I, P]),
             }
@@ -177,6 +178,14 @@ def sgemm_diag_tf32_mma_rate(iters: int = 20000):
     current device (synchronous, about 6 ms)."""
     v = ctypes.c_double(0.0)
     st = lib().sgemm_diag_tf32_mma_rate(iters, ctypes.byref(v))
+    return st, v.value
+
+
+def sgemm_diag_tf32_pair_mma_rate(iters: int = 20000):
+    """(status, TFLOP/s): the same for two-SM (cta_group::2) MMAs issued by
+    CTA pairs."""
+    v = ctypes.c_double(0.0)
+    st = lib().sgemm_diag_tf32_pair_mma_rate(iters, ctypes.byref(v))
     return st, v.value
 
 

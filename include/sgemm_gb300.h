@@ -299,6 +299,16 @@ long long sgemm_set_wait_timeout_ns(long long ns);
 int sgemm_diag_tf32_mma_rate(int iters, double* tflops);
 
 /*
+ * Diagnostic: the same measurement for the pair form the 3xTF32 path runs by
+ * default. Clusters of two CTAs (as many as are resident at once); the even
+ * CTA issues `iters` x 4 tcgen05.mma.cta_group::2.kind::tf32 of M 256 (128
+ * rows per CTA), N 256 (half of B in each CTA), K 8. The rate counts the
+ * multiply-adds of all SMs taking part. Same arguments, errors and duration
+ * as sgemm_diag_tf32_mma_rate.
+ */
+int sgemm_diag_tf32_pair_mma_rate(int iters, double* tflops);
+
+/*
  * The same C = alpha * A * B + beta * C as sgemm(), with the same arguments,
  * checks and results, for callers that must not allocate device memory: code
  * running while a stream is captured into a graph, applications whose memory

@@ -84,3 +84,4 @@ def test_config_registry():
 def test_tf32_rate_probe_rejects_bad_arguments():
     # checked on the host before any device call
     assert binding.sgemm_diag_tf32_mma_rate(0)[0] == binding.SGEMM_ERR_INVALID_VALUE
+    assert binding.sgemm_diag_tf32_pair_mma_rate(0)[0] == binding.SGEMM_ERR_INVALID_VALUE
