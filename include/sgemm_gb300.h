@@ -206,7 +206,10 @@ int sgemm_last_config(char* buf, int len);
  * (device, stream) workspace: SGEMM_OK, or SGEMM_ERR_DEVICE_TIMEOUT if a
  * kernel gave up on a bounded wait since the last poll. *detail (if not NULL)
  * receives the device-side code (1 = operand tile, 2 = slot release, 3 =
- * split partial, 4 = CTA rendezvous). SGEMM_ERR_LAUNCH if synchronising fails.
+ * split partial, 4 = CTA rendezvous, 5 = the two CTAs of a two-SM pair of
+ * sgemm_3xtf32 got different tensor-memory columns; none of them is a device
+ * fault, and the context stays usable). SGEMM_ERR_LAUNCH if synchronising
+ * fails.
  */
 int sgemm_poll_device_status(void* stream, int* detail);
 
