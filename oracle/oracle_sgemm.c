@@ -25,7 +25,7 @@
  * ascending k in double. On integer inputs whose partial sums stay far below
  * 2^53 the result is therefore exact.
  *
- * Readings where the pages are silent (listed in the design notes as well):
+ * Readings where the pages are silent:
  *   - beta == 0: C is not read at all (so NaN or garbage in C cannot leak in);
  *   - alpha == 0 or K == 0: A and B are not read; the result is beta * C.
  *
