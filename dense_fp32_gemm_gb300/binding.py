@@ -270,8 +270,8 @@ def sgemm_ladder(kernel, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=No
 LADDER_KERNELS = (3, 7, 8)
 
 
-SGEMM_X3_SINGLE, SGEMM_X3_PAIR, SGEMM_X3_PAIR_MULTICAST = 1, 2, 3
-X3_FORMS = (SGEMM_X3_PAIR, SGEMM_X3_PAIR_MULTICAST, SGEMM_X3_SINGLE)
+SGEMM_X3_SINGLE, SGEMM_X3_PAIR = 1, 2
+X3_FORMS = (SGEMM_X3_PAIR, SGEMM_X3_SINGLE)
 
 
 X3_PLAN_FIELDS = ("form", "bk", "stages", "ctas", "units", "dp_units", "split_units", "kiters")
@@ -285,9 +285,8 @@ def sgemm_3xtf32_plan(M: int, N: int, K: int, form: int, pairs: int, sms: int):
 
 
 def sgemm_3xtf32_set_kernel_form(form: int) -> int:
-    """SGEMM_X3_PAIR (default): CTA pairs with two-SM MMAs; SGEMM_X3_PAIR_MULTICAST:
-    CTA pairs sharing B tiles by multicast; SGEMM_X3_SINGLE: single CTAs.
-    Returns the previous setting (or an error status)."""
+    """SGEMM_X3_PAIR (default): CTA pairs with two-SM MMAs; SGEMM_X3_SINGLE: single
+    CTAs. Returns the previous setting (or an error status)."""
     return lib().sgemm_3xtf32_set_kernel_form(form)
 
 

@@ -88,18 +88,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// The same 2-D box delivered to the shared memory of every CTA of the cluster
-// whose bit is set in `cta_mask`, at the same CTA-relative offset `dst`; each
-// destination's mbarrier at offset `bar` receives the box's transaction bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, int x,
-                                                      int y, uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // Orders this thread's earlier generic-proxy writes to shared memory before
 // later async-proxy reads of it (TMA stores, tensor-core operand reads) that
 // are ordered after this point through a barrier.

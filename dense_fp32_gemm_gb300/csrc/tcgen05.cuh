@@ -74,16 +74,6 @@ __device__ __forceinline__ void commit(uint32_t mbar_smem) {
       : "memory");
 }
 
-// The same, arriving on the mbarrier at offset `mbar_smem` in every CTA of the
-// cluster whose bit is set in `cta_mask`.
-__device__ __forceinline__ void commit_multicast(uint32_t mbar_smem, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(mbar_smem),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // ---- the pair form (cta_group::2) ------------------------------------------
 // D[tmem] (+)= A * B for an M = 256 tile spread over a CTA pair, issued by one
 // thread of the even CTA: A rows 0-127 come from that CTA's shared memory and

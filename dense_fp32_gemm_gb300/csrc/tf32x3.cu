@@ -40,10 +40,8 @@
 //     converters of both CTAs are done (the odd CTA's through one relayed
 //     remote arrival per stage); its commits free the stage and publish the
 //     accumulator in both CTAs; its MMA thread waits for both epilogues.
-//   * multicast pairs: the same tile pairs, each CTA loading its A tile and
-//     one half of the B tile into both CTAs by TMA multicast and issuing its
-//     own M = 128 MMAs; a stage is refilled once both CTAs' MMAs read it.
 //   * single CTAs, each with its own A and B tiles.
+// Each CTA loads only its own tiles; no TMA load is multicast.
 // Before exiting, a CTA of a pair waits (bounded) until its barriers have
 // received the peer's last arrivals, then meets the peer at a cluster
 // barrier (two-SM pairs free their TMEM together after it).
@@ -91,7 +89,8 @@ constexpr int kMaxStages = 6;
 // (4096^3: 251 against 226 TFLOP/s), 32 below (8191 x 1000 x 777: 99 against
 // 86 TFLOP/s). B_PARTS = 2 (the two-SM form): a CTA holds half of each B
 // tile, and BK = 32 gives three 64 KB stages (its hand-offs between the CTAs
-// of a pair cost more, so it always takes 32).
+// of a pair cost more, so it always takes 32; 16-wide stages measured 158
+// against 265 TFLOP/s at 4096^3).
 template <int BK_, int B_PARTS = 1>
 struct Slice {
   static constexpr int BK = BK_;
@@ -106,18 +105,16 @@ struct Slice {
 };
 static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
                   Slice<32>::ST * Slice<32>::STAGE_BYTES == kStageRegion &&
-                  Slice<16, 2>::ST * Slice<16, 2>::STAGE_BYTES == kStageRegion &&
                   Slice<32, 2>::ST * Slice<32, 2>::STAGE_BYTES == kStageRegion &&
-                  Slice<16, 2>::ST <= kMaxStages,
+                  Slice<16>::ST <= kMaxStages,
               "every width fills the same stage region");
 constexpr int ACC_COLS = BN;              // one FP32 accumulator: 128 lanes x BN columns
 constexpr int NBUF = 2;                   // accumulators, so the epilogue overlaps the next MMAs
 constexpr int TMEM_COLS = NBUF * ACC_COLS;  // all 512 columns
 // Kernel forms (the values sgemm_3xtf32_set_kernel_form takes): single CTAs;
 // CTA pairs whose even CTA issues M = 256 MMAs over both (cta_group::2),
-// each CTA holding half of every B tile; CTA pairs that share B tiles by
-// multicast, each CTA issuing its own M = 128 MMAs.
-enum Form : int { kSingle = 1, kTwoSmPair = 2, kMulticastPair = 3 };
+// each CTA holding half of every B tile.
+enum Form : int { kSingle = 1, kTwoSmPair = 2 };
 constexpr int EPI_THREADS = 128;          // warps 2-5
 constexpr int CONV_WARP0 = 6;             // warps 6-9 write the residual tiles
 constexpr int CONV_THREADS = 128;
@@ -234,9 +231,9 @@ __global__ void __launch_bounds__(NT, 1)
   volatile int* abort_w = &bar->abort;
   const uint32_t base_addr = ptx::smem_addr(base);
 
-  static_assert(FORM == kSingle || FORM == kMulticastPair || FORM == kTwoSmPair, "form");
+  static_assert(FORM == kSingle || FORM == kTwoSmPair, "form");
   constexpr bool TWO_SM = FORM == kTwoSmPair;
-  constexpr int CL = FORM == kSingle ? 1 : 2;       // CTAs per cluster
+  constexpr int CL = TWO_SM ? 2 : 1;                // CTAs per cluster
   constexpr int CG = TWO_SM ? 2 : 1;                // cta_group of every tcgen05 instruction
   using S = Slice<BK, TWO_SM ? 2 : 1>;
   constexpr int ST = S::ST, ROW_BYTES = S::ROW_BYTES;
@@ -259,7 +256,7 @@ __global__ void __launch_bounds__(NT, 1)
       ptx::mbar_init(ptx::smem_addr(&bar->full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&bar->conv[s]),
                      CONV_THREADS / 32 + ((TWO_SM && rank == 0) ? 1 : 0));
-      ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), TWO_SM ? 1 : CL);
+      ptx::mbar_init(ptx::smem_addr(&bar->empty[s]), 1);
     }
     for (int i = 0; i < NBUF; ++i) {
       ptx::mbar_init(ptx::smem_addr(&bar->tmem_full[i]), 1);
@@ -278,7 +275,8 @@ __global__ void __launch_bounds__(NT, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
-  // the peer's barriers must be initialised before anything is multicast to them
+  // the peer's barriers must be initialised before the pair's first remote
+  // arrival or commit reaches them
   if (CL == 2) ptx::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem = bar->tmem_addr;
@@ -315,16 +313,11 @@ __global__ void __launch_bounds__(NT, 1)
           const uint32_t st0 = base_addr + (uint32_t)(s * STAGE_BYTES);
           ptx::mbar_arrive_expect_tx(fb, (uint32_t)(A_BYTES + B_BYTES));
           ptx::tma_load_2d(st0, &tmA, kb * BK, tm * BM, fb);
-          if (CL == 1) {
-            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN, fb);
-          } else if (TWO_SM) {
+          if (TWO_SM) {
             // this CTA's half of the B tile (N columns 128 * rank ..), into this CTA
             ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN + rank * (BN / 2), fb);
           } else {
-            // this CTA's half of the B tile, into both CTAs
-            const uint32_t half = (uint32_t)(rank * (B_BYTES / 2));
-            const int row = tn * BN + rank * (BN / 2);
-            ptx::tma_load_2d_multicast(st0 + 2 * A_BYTES + half, &tmB, kb * BK, row, fb, kPair);
+            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN, fb);
           }
         }
         if (!ok) break;
@@ -338,9 +331,8 @@ __global__ void __launch_bounds__(NT, 1)
           if ((long long)(ptx::global_ns() - t0) > cleanup_bound_ns(p.timeout_ns)) break;
       }
       if (CL == 2) {
-        // the peer's MMA warp (the even CTA's, in the two-SM form) arrives on
-        // this CTA's empty barriers: wait (bounded) for its arrivals on the
-        // last use of every stage
+        // the even CTA's MMA commits arrive on this CTA's empty barriers: wait
+        // (bounded) for its arrivals on the last use of every stage
         for (int j = it; j < it + ST; ++j) {
           const uint32_t eb = ptx::smem_addr(&bar->empty[j % ST]);
           while (!ptx::mbar_try_wait(eb, (uint32_t)((j / ST) & 1) ^ 1u))
@@ -429,10 +421,8 @@ __global__ void __launch_bounds__(NT, 1)
           // frees the stage (in both CTAs of a pair) once these MMAs are done
           if (TWO_SM)
             tc::commit_pair_multicast(ptx::smem_addr(&bar->empty[s]), kPair);
-          else if (CL == 1)
-            tc::commit(ptx::smem_addr(&bar->empty[s]));
           else
-            tc::commit_multicast(ptx::smem_addr(&bar->empty[s]), kPair);
+            tc::commit(ptx::smem_addr(&bar->empty[s]));
         }
         if (!ok) break;
         // the piece's accumulator is ready (in both CTAs, in the two-SM form)
@@ -649,8 +639,6 @@ __global__ void __launch_bounds__(NT, 1)
       tc::fence_after_sync();
       tc::tmem_dealloc(tmem, TMEM_COLS);
     }
-    // neither CTA of a pair leaves while the other may still write to it
-    if (CL == 2) ptx::cluster_sync();
   }
 }
 
@@ -659,7 +647,7 @@ __global__ void __launch_bounds__(NT, 1)
 std::mutex g_mutex;
 bool g_ready[64];
 int g_pairs[64];          // resident clusters of two; 0 = the pair form cannot run
-// the requested Form; the pair forms run where possible
+// the requested Form; the pair form runs where possible
 std::atomic<int> g_form{kTwoSmPair};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_tried = false;
@@ -676,7 +664,7 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   Plan pl{};
   pl.form = (want != kSingle && pairs > 0) ? want : (int)kSingle;
   // schedule: whole tiles, then the last one to two waves split along K. In
-  // the pair forms a schedule unit is two vertically adjacent tiles (a tile
+  // the pair form a schedule unit is two vertically adjacent tiles (a tile
   // row pair), handed to one cluster.
   const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
   // the k-slice width (see Slice). The two-SM form always takes 32: its
@@ -690,8 +678,8 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
     // 305 TFLOP/s with 4, 298 with 2; 16 the same as 8)
     pl.sched = make_schedule((tiles_m + 1) / 2, tiles_n, pl.kiters, pairs, 8, 64 / pl.bk);
     // every tile split along K: the pairs' lockstep costs more than they save
-    // (measured in both pair forms at 1024^3, 1024 x 1024 x 16384 and
-    // 16384 x 64 x 4096; the two-SM form gained 4 % at 2048^3 only)
+    // (measured at 1024^3, 1024 x 1024 x 16384 and 16384 x 64 x 4096; the
+    // two-SM form gained 4 % at 2048^3 only)
     if (pl.sched.dp_tiles == 0) pl.form = kSingle;
   }
   if (pl.form == kSingle) {
@@ -772,9 +760,6 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
       using namespace x3;
       if (cudaFuncSetAttribute(gemm_kernel<kSingle, 16>, attr, SMEM_BYTES) != cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kSingle, 32>, attr, SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(gemm_kernel<kMulticastPair, 16>, attr, SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(gemm_kernel<kMulticastPair, 32>, attr, SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(gemm_kernel<kTwoSmPair, 16>, attr, SMEM_BYTES) != cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kTwoSmPair, 32>, attr, SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
@@ -792,20 +777,12 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
       qc.dynamicSmemBytes = x3::SMEM_BYTES;
       qc.attrs = qa;
       qc.numAttrs = 1;
-      // every pair kernel has the same block and shared-memory size; take the smallest
-      int n[4] = {0, 0, 0, 0};
-      if (cudaOccupancyMaxActiveClusters(&n[0], gemm_kernel<kMulticastPair, 16>, &qc) !=
-              cudaSuccess ||
-          cudaOccupancyMaxActiveClusters(&n[1], gemm_kernel<kMulticastPair, 32>, &qc) !=
-              cudaSuccess ||
-          cudaOccupancyMaxActiveClusters(&n[2], gemm_kernel<kTwoSmPair, 16>, &qc) != cudaSuccess ||
-          cudaOccupancyMaxActiveClusters(&n[3], gemm_kernel<kTwoSmPair, 32>, &qc) != cudaSuccess) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<kTwoSmPair, 32>, &qc) != cudaSuccess) {
         cudaGetLastError();
-        n[0] = 0;
+        n = 0;
       }
-      int least = n[0];
-      for (int j = 1; j < 4; ++j) least = n[j] < least ? n[j] : least;
-      x3::g_pairs[dev] = least;
+      x3::g_pairs[dev] = n;
       x3::g_ready[dev] = true;
     }
     pairs = x3::g_pairs[dev];
@@ -893,14 +870,8 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     lc.stream = stream;
     lc.attrs = la;
     lc.numAttrs = 1;
-    using namespace x3;
-    cudaError_t e;
-    if (form == kTwoSmPair)
-      e = bk == 16 ? cudaLaunchKernelEx(&lc, gemm_kernel<kTwoSmPair, 16>, p, mA, mB)
-                   : cudaLaunchKernelEx(&lc, gemm_kernel<kTwoSmPair, 32>, p, mA, mB);
-    else
-      e = bk == 16 ? cudaLaunchKernelEx(&lc, gemm_kernel<kMulticastPair, 16>, p, mA, mB)
-                   : cudaLaunchKernelEx(&lc, gemm_kernel<kMulticastPair, 32>, p, mA, mB);
+    // the two-SM form always runs 32-wide slices (make_plan)
+    const cudaError_t e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kTwoSmPair, 32>, p, mA, mB);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return SGEMM_ERR_LAUNCH;
@@ -910,7 +881,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   snprintf(text, sizeof(text),
            "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d%s grid=%d units=%d dp=%d split=%d kiters=%d%s",
            x3::BM, x3::BN, bk, (form == x3::kTwoSmPair ? 96 : 64) / bk, CL,
-           form == x3::kTwoSmPair ? " pair=2sm" : (form == x3::kMulticastPair ? " pair=multicast" : ""),
+           form == x3::kTwoSmPair ? " pair=2sm" : "",
            ctas, sched.grid, sched.dp_tiles,
            sched.tiles - sched.dp_tiles, kiters, a_direct ? "" : " a=copied");
   note_last_config(text);
@@ -919,8 +890,8 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
 
 SGEMM_API int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sms, int* out) {
   if (M < 1 || N < 1 || K < 1) return SGEMM_ERR_INVALID_DIM;
-  if ((form != SGEMM_X3_SINGLE && form != SGEMM_X3_PAIR && form != SGEMM_X3_PAIR_MULTICAST) ||
-      pairs < 0 || sms < 1 || out == nullptr)
+  if ((form != SGEMM_X3_SINGLE && form != SGEMM_X3_PAIR) || pairs < 0 || sms < 1 ||
+      out == nullptr)
     return SGEMM_ERR_INVALID_VALUE;
   const x3::Plan pl = x3::make_plan(M, N, K, form, pairs, sms);
   out[0] = pl.form;
@@ -935,7 +906,6 @@ SGEMM_API int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sm
 }
 
 SGEMM_API int sgemm_3xtf32_set_kernel_form(int form) {
-  if (form != SGEMM_X3_SINGLE && form != SGEMM_X3_PAIR && form != SGEMM_X3_PAIR_MULTICAST)
-    return SGEMM_ERR_INVALID_VALUE;
+  if (form != SGEMM_X3_SINGLE && form != SGEMM_X3_PAIR) return SGEMM_ERR_INVALID_VALUE;
   return x3::g_form.exchange(form);
 }

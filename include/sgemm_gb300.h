@@ -108,18 +108,16 @@ int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, cons
  *     128 x 256 tiles; the even CTA issues M = 256 MMAs over both
  *     (tcgen05 cta_group::2), each CTA holding its A tile and half of the B
  *     tile in shared memory and its 128 rows of the accumulator in TMEM;
- *   SGEMM_X3_PAIR_MULTICAST: clusters of two CTAs on the same tiles that share
- *     each B tile through TMA multicast, each issuing its own M = 128 MMAs;
- *   SGEMM_X3_SINGLE: single CTAs, each loading its own B tiles.
- * The pair forms run where the device can co-schedule CTA pairs and the
- * problem has at least two waves of whole tile pairs, else single CTAs. All
- * give the same results within the tolerance (bit-identical on integer
- * inputs). Returns the previous setting, or SGEMM_ERR_INVALID_VALUE (nothing
- * changed) for another value.
+ *   SGEMM_X3_SINGLE: single CTAs, each loading its own A and B tiles.
+ * In both forms every CTA loads only its own tiles (no TMA load is shared
+ * between CTAs). The pair form runs where the device can co-schedule CTA
+ * pairs and the problem has at least two waves of whole tile pairs, else
+ * single CTAs. Both give the same results within the tolerance (bit-identical
+ * on integer inputs). Returns the previous setting, or
+ * SGEMM_ERR_INVALID_VALUE (nothing changed) for another value.
  */
 #define SGEMM_X3_SINGLE 1
 #define SGEMM_X3_PAIR 2
-#define SGEMM_X3_PAIR_MULTICAST 3
 int sgemm_3xtf32_set_kernel_form(int form);
 
 /*
@@ -128,7 +126,7 @@ int sgemm_3xtf32_set_kernel_form(int form);
  * many CTA pairs the device keeps resident (0: none), `sms` its SM count.
  * out = {form that runs, k-slice width, stages, CTAs, schedule units (a CTA
  * pair each in the pair forms), whole-tile units, K-split units, k-slices}.
- * The pair forms fall back to single CTAs when pairs == 0 or when every tile
+ * The pair form falls back to single CTAs when pairs == 0 or when every tile
  * would be split along K. Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM unless
  * M, N, K >= 1 (only such problems launch the GEMM kernel), or
  * SGEMM_ERR_INVALID_VALUE for another form, pairs < 0, sms < 1 or a NULL out.

@@ -57,11 +57,10 @@ def test_validation_happens_before_any_device_call():
         assert binding.sgemm_ladder(k, 4, 4, 4, 1.0, 16, 4, 16, 3, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_LD
         assert binding.sgemm_ladder(k, 4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 17, 4, None) == binding.SGEMM_ERR_MISALIGNED
         assert binding.sgemm_ladder(k, 0, 4, 4, 1.0, 0, 4, 0, 4, 0.0, 0, 4, None) == binding.SGEMM_OK
-    assert binding.sgemm_3xtf32_set_kernel_form(4) == binding.SGEMM_ERR_INVALID_VALUE
-    assert binding.sgemm_3xtf32_set_kernel_form(0) == binding.SGEMM_ERR_INVALID_VALUE
+    for form in (0, 3, 4):
+        assert binding.sgemm_3xtf32_set_kernel_form(form) == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_3xtf32_set_kernel_form(binding.SGEMM_X3_SINGLE) == binding.SGEMM_X3_PAIR
-    assert binding.sgemm_3xtf32_set_kernel_form(binding.SGEMM_X3_PAIR_MULTICAST) == binding.SGEMM_X3_SINGLE
-    assert binding.sgemm_3xtf32_set_kernel_form(binding.SGEMM_X3_PAIR) == binding.SGEMM_X3_PAIR_MULTICAST
+    assert binding.sgemm_3xtf32_set_kernel_form(binding.SGEMM_X3_PAIR) == binding.SGEMM_X3_SINGLE
     assert binding.sgemm_host_set_pipeline(-1, 0, 0, 0) == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_host_set_pipeline(0, 0, 0, 9) == binding.SGEMM_ERR_INVALID_VALUE
     for k in (0, 1, 6, 9):

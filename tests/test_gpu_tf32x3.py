@@ -2,8 +2,8 @@
 bar as the FFMA path -- bit-exact on integer inputs, the FP32 tolerance
 |C - C_ref| <= 1e-5 * (|alpha| sum |a||b| + |beta| |c|) + 1e-30 on real inputs --
 on small shapes element by element and on the full workloads by sampling.
-Every test runs in the three kernel forms: CTA pairs with two-SM MMAs (the
-default), CTA pairs sharing B tiles by multicast, and single CTAs."""
+Every test runs in both kernel forms: CTA pairs with two-SM MMAs (the
+default) and single CTAs."""
 import numpy as np
 import pytest
 import torch
@@ -19,11 +19,10 @@ X3 = binding.sgemm_3xtf32
 
 
 FORM_TEXT = {binding.SGEMM_X3_PAIR: "cluster=2 pair=2sm",
-             binding.SGEMM_X3_PAIR_MULTICAST: "cluster=2 pair=multicast",
              binding.SGEMM_X3_SINGLE: "cluster=1 "}
 
 
-@pytest.fixture(autouse=True, params=binding.X3_FORMS, ids=["pair2sm", "multicast", "single"])
+@pytest.fixture(autouse=True, params=binding.X3_FORMS, ids=["pair2sm", "single"])
 def kernel_form(request):
     prev = binding.sgemm_3xtf32_set_kernel_form(request.param)
     yield request.param
@@ -106,11 +105,10 @@ def test_slice_width_follows_k(kernel_form):
     H.check_against_oracle(Workload("x3k", 200, 300, 1024, 1.0, 0.5, "int3", 38), fn=X3)
     assert "128x256x16_s4" in binding.sgemm_last_config()
     # whole waves of tile pairs at K = 1024: the two-SM form keeps BK = 32
-    # (three stages of half B tiles), the multicast form takes BK = 16
+    # (three stages of half B tiles), single CTAs take BK = 16
     H.check_sampled(Workload("x3k2", 128 * 2 * 76 * 2, 256, 1024, 1.0, 0.5, "int3", 39),
                     rows=32, elements=2048, fn=X3)
-    want = {binding.SGEMM_X3_PAIR: "128x256x32_s3", binding.SGEMM_X3_PAIR_MULTICAST: "128x256x16_s4",
-            binding.SGEMM_X3_SINGLE: "128x256x16_s4"}[kernel_form]
+    want = {binding.SGEMM_X3_PAIR: "128x256x32_s3", binding.SGEMM_X3_SINGLE: "128x256x16_s4"}[kernel_form]
     assert want in binding.sgemm_last_config()
 
 

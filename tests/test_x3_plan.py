@@ -1,6 +1,6 @@
 """The dispatch plan of sgemm_3xtf32 on the host (no GPU): which kernel form
 runs, the k-slice width, the stages and the persistent schedule. The pair
-forms fall back to single CTAs when the device keeps no CTA pairs resident or
+form falls back to single CTAs when the device keeps no CTA pairs resident or
 when every tile would be split along K; the two-SM form always takes 32-wide
 slices (three stages of half B tiles), single CTAs 16 from K = 1024 up and 32
 below. The GB300 figures (152 SMs, 76 resident pairs) are the ones the GPU
@@ -10,7 +10,7 @@ import pytest
 from dense_fp32_gemm_gb300 import binding
 
 SMS, PAIRS = 152, 76
-PAIR, MCAST, SINGLE = binding.SGEMM_X3_PAIR, binding.SGEMM_X3_PAIR_MULTICAST, binding.SGEMM_X3_SINGLE
+PAIR, SINGLE = binding.SGEMM_X3_PAIR, binding.SGEMM_X3_SINGLE
 
 
 def plan(M, N, K, form, pairs=PAIRS, sms=SMS):
@@ -24,14 +24,12 @@ def test_square4096_in_each_form():
     p = plan(4096, 4096, 4096, PAIR)
     assert (p["form"], p["bk"], p["stages"], p["ctas"], p["units"]) == (PAIR, 32, 3, 152, 76)
     assert (p["dp_units"], p["split_units"], p["kiters"]) == (152, 104, 128)
-    p = plan(4096, 4096, 4096, MCAST)
-    assert (p["form"], p["bk"], p["stages"], p["ctas"], p["kiters"]) == (MCAST, 16, 4, 152, 256)
     p = plan(4096, 4096, 4096, SINGLE)
     assert (p["form"], p["bk"], p["stages"], p["ctas"], p["units"]) == (SINGLE, 16, 4, 152, 152)
     assert (p["dp_units"], p["split_units"]) == (304, 208)
 
 
-@pytest.mark.parametrize("form", [PAIR, MCAST])
+@pytest.mark.parametrize("form", [PAIR, SINGLE])
 def test_pairs_fall_back_when_every_tile_is_split(form):
     # 2048^3: 32 tile pairs on 76 clusters, all split along K
     p = plan(2048, 2048, 2048, form)
@@ -39,9 +37,8 @@ def test_pairs_fall_back_when_every_tile_is_split(form):
     assert p["dp_units"] == 0
 
 
-@pytest.mark.parametrize("form", [PAIR, MCAST])
-def test_pairs_fall_back_without_resident_pairs(form):
-    p = plan(4096, 4096, 4096, form, pairs=0)
+def test_pairs_fall_back_without_resident_pairs():
+    p = plan(4096, 4096, 4096, PAIR, pairs=0)
     assert p["form"] == SINGLE and p["ctas"] == SMS
 
 
@@ -60,7 +57,7 @@ def test_two_sm_form_keeps_32_wide_slices_at_any_k():
 def test_schedule_covers_every_tile():
     # whole-tile units plus the tiles behind the K-split units cover the grid of tiles
     for (M, N, K, form) in [(4096, 4096, 4096, PAIR), (8192, 8192, 8192, PAIR), (8191, 1000, 777, SINGLE),
-                            (16384, 64, 4096, SINGLE), (1000, 1300, 2056, MCAST)]:
+                            (16384, 64, 4096, SINGLE), (1000, 1300, 2056, PAIR)]:
         p = plan(M, N, K, form)
         tiles_m, tiles_n = -(-M // 128), -(-N // 256)
         units = tiles_n * (-(-tiles_m // 2) if p["form"] != SINGLE else tiles_m)
@@ -72,6 +69,9 @@ def test_argument_errors():
     assert binding.sgemm_3xtf32_plan(0, 4, 4, PAIR, PAIRS, SMS)[0] == binding.SGEMM_ERR_INVALID_DIM
     assert binding.sgemm_3xtf32_plan(4, 4, 0, PAIR, PAIRS, SMS)[0] == binding.SGEMM_ERR_INVALID_DIM
     assert binding.sgemm_3xtf32_plan(4, 4, 4, 0, PAIRS, SMS)[0] == binding.SGEMM_ERR_INVALID_VALUE
-    assert binding.sgemm_3xtf32_plan(4, 4, 4, 4, PAIRS, SMS)[0] == binding.SGEMM_ERR_INVALID_VALUE
+    # 3 named a form that shared B tiles between the CTAs of a pair by TMA
+    # multicast; it is no longer built and is rejected like any unknown form
+    for form in (3, 4):
+        assert binding.sgemm_3xtf32_plan(4, 4, 4, form, PAIRS, SMS)[0] == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_3xtf32_plan(4, 4, 4, PAIR, -1, SMS)[0] == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_3xtf32_plan(4, 4, 4, PAIR, PAIRS, 0)[0] == binding.SGEMM_ERR_INVALID_VALUE
