@@ -13,6 +13,13 @@ independent replicas (the path has no exchange step). `e2e` times the same
 work from pinned host buffers: H2D of A, B, C, the call, D2H of C.
 `--impl reference` times the CPU oracle (FP64 triple loop) on a bounded row
 sample of the same workload; it runs on rank 0 only.
+
+Besides the contract's keys the line carries the per-step statistics of the K
+event-timed steps (mean, median, min, max, spread), the SM clock and clock-event
+reasons sampled through NVML inside the timed window, and -- from the CPU
+baseline leg, which computes the oracle's rows anyway -- `verified`: one call
+of each timed path on a fresh C before any timing, checked against the oracle
+on those rows and on sampled elements at the FP32 tolerance.
 """
 from __future__ import annotations
 
@@ -24,7 +31,6 @@ import glob
 import hashlib
 import json
 import os
-import re
 import subprocess
 import sys
 import time
@@ -121,23 +127,43 @@ def measured_peaks():
         return {}
 
 
-def profiled_traffic(workload, tile_config):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    or None if there is none, the kernel sources changed since, or the
-    summary was taken on another tile configuration."""
-    path = os.path.join(ROOT, "profiles", f"ffma_sgemm_{workload}.md")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def profiled_traffic(workload, tile_config, path=TRAFFIC_PATH):
+    """DRAM bytes per launch of the FFMA kernel on this workload, from the
+    committed ncu figures (profiles/traffic.json: one entry per workload with
+    the kernel-source hash and tile configuration it was captured on), or None
+    if there is none, the kernel sources changed since, or it was taken on
+    another tile configuration."""
     try:
-        text = open(path).read()
-    except OSError:
+        table = json.load(open(path))
+    except (OSError, ValueError):
         return None
-    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    c = re.search(r"tile_config:\s*(\S+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash():
+    e = table.get("ffma_sgemm", {}).get(workload)
+    if not isinstance(e, dict):
         return None
-    if not c or not tile_config.startswith(c.group(1)):
+    if e.get("kernel_source_sha") != kernel_source_hash():
         return None
-    return float(m.group(1))
+    if not e.get("tile_config") or not tile_config.startswith(e["tile_config"]):
+        return None
+    try:
+        return float(e["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
+        return None
+
+
+def step_stats(ms):
+    """Mean, median, min, max and spread (max - min over the median, %) of
+    per-step device times in milliseconds."""
+    v = sorted(float(x) for x in ms)
+    if not v:
+        return None
+    n = len(v)
+    med = v[n // 2] if n % 2 else 0.5 * (v[n // 2 - 1] + v[n // 2])
+    return {"mean": round(sum(v) / n, 5), "median": round(med, 5), "min": round(v[0], 5),
+            "max": round(v[-1], 5), "spread_pct": round(100.0 * (v[-1] - v[0]) / med, 2) if med else None,
+            "n": n}
 
 
 # ---- NVTX ranges: name the bench's phases in profiler timelines ------------------------
@@ -152,8 +178,113 @@ def nvtx_range(name):
 
 
 # ---- clocks -------------------------------------------------------------------------
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*) that hold the
+# SM clock below what was asked for.
+NVML_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+NVML_CLOCK_SM = 1
+
+
+def summarize_clock_samples(samples, t0, t1, max_mhz, source, period_ms=None):
+    """samples: (wall time, SM MHz, reason bits or None). Only the samples
+    taken inside [t0, t1] count; with none inside, the clock is unknown."""
+    inside = [x for x in samples if t0 <= x[0] <= t1]
+    out = {"sm_mhz": None, "sm_max_mhz": max_mhz, "samples": len(inside), "reasons": [],
+           "source": source}
+    if period_ms is not None:
+        out["period_ms"] = period_ms
+    if not inside:
+        out["reasons"] = ["no clock sample inside the timed window"]
+        return out
+    mhz = sorted(x[1] for x in inside)
+    n = len(mhz)
+    out["sm_mhz"] = mhz[n // 2] if n % 2 else 0.5 * (mhz[n // 2 - 1] + mhz[n // 2])
+    out["sm_mhz_min"] = mhz[0]
+    out["reasons"] = sorted({name for x in inside if x[2] is not None
+                             for bit, name in NVML_REASON_BITS.items() if x[2] & bit})
+    return out
+
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons of one GPU, read through NVML by a
+    background thread every `period_s` seconds. The queries only read: no
+    clock, limit or mode is set. `lib` replaces libnvidia-ml (tests)."""
+
+    def __init__(self, pci_bus_id=None, index=0, period_s=0.002, lib=None):
+        import ctypes
+        import threading
+        self.samples, self.err, self.period_s = [], None, period_s
+        self._stop = threading.Event()
+        self._thread = None
+        self.lib, self.max_mhz = None, None
+        try:
+            nv = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            if pci_bus_id:
+                rc = nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h))
+            else:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(index)), ctypes.byref(h))
+            if rc != 0:
+                raise OSError(f"no NVML device handle (status {rc})")
+            self._reasons = (getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                             or nv.nvmlDeviceGetCurrentClocksThrottleReasons)
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.lib, self.h = nv, h
+        except (OSError, AttributeError) as e:
+            self.err = str(e)
+
+    def poll(self):
+        """One sample: (wall time, SM MHz, reason bits or None), or None."""
+        import ctypes
+        clk, bits = ctypes.c_uint(), ctypes.c_ulonglong()
+        t = time.time()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, NVML_CLOCK_SM, ctypes.byref(clk)) != 0:
+            return None
+        r = int(bits.value) if self._reasons(self.h, ctypes.byref(bits)) == 0 else None
+        return (t, float(clk.value), r)
+
+    def _run(self):
+        while not self._stop.is_set():
+            x = self.poll()
+            if x is not None:
+                self.samples.append(x)
+            self._stop.wait(self.period_s)
+
+    def start(self):
+        import threading
+        if self.lib is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        if self.lib is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": [f"NVML unavailable: {self.err}"], "source": "nvml"}
+        return summarize_clock_samples(self.samples, t0, t1, self.max_mhz, "nvml",
+                                       period_ms=round(self.period_s * 1e3, 3))
+
+
+def nvml_bus_id(props):
+    """NVML's PCI bus id ("domain:bus:device.0") of a torch device, or None."""
+    try:
+        return f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    except AttributeError:
+        return None
+
+
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while it runs."""
+    """nvidia-smi sampling of SM clock and throttle reasons while it runs (used
+    when NVML cannot be loaded)."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -193,9 +324,10 @@ class ClockSampler:
                 rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
             except ValueError:
                 continue
-        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        inside = [r for r in rows if t0 <= r[0] <= t1]
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": ["no clock sample inside the timed window"]}
         mhz = sorted(r[1] for r in inside)
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4]) if v == "Active"})
@@ -241,37 +373,96 @@ def aggregate(flops_per_step_per_rank, steps, seconds_max, world):
 
 
 # ---- CPU oracle timing --------------------------------------------------------------
-def oracle_rows_timing(w, A, B, C, rows, threads):
+def oracle_rows_timing(w, A, B, C, rows, threads, keep=False):
+    """Seconds the oracle takes for the first `rows` rows of C; with keep,
+    also the rows it computed (reference values and magnitudes)."""
     import oracle
     Cn = None if w.beta == 0 else C.numpy()
     t0 = time.perf_counter()
-    oracle.sgemm_rows(w.M, w.N, w.K, w.alpha, A.numpy(), w.LDA, B.numpy(), w.LDB, w.beta, Cn,
-                      w.LDC, 0, rows, threads=threads)
-    return time.perf_counter() - t0
+    ref = oracle.sgemm_rows(w.M, w.N, w.K, w.alpha, A.numpy(), w.LDA, B.numpy(), w.LDB, w.beta, Cn,
+                            w.LDC, 0, rows, threads=threads)
+    dt = time.perf_counter() - t0
+    return (dt, ref) if keep else dt
 
 
-def cpu_baseline(w, A, B, C, budget_s=10.0):
+TOL_REL, TOL_ABS = 1e-5, 1e-30
+TOLERANCE_RULE = "|C - C_ref| <= 1e-5 * (|alpha| sum_k |a_ik b_kj| + |beta| |c_ij|) + 1e-30"
+
+
+def check_against_reference(gpu_rows, ref, mag, exact):
+    """Compare GPU results with oracle values (float64 arrays of one shape):
+    every element within the FP32 tolerance, and bit-exact (as floats) when
+    `exact` (integer inputs). Returns (ok, worst error / bound, mismatches)."""
+    import numpy as np
+    g = np.asarray(gpu_rows, dtype=np.float64)
+    err = np.abs(g - ref)
+    bound = TOL_REL * mag + TOL_ABS
+    ok = np.isfinite(g) & (err <= bound)
+    if exact:
+        ok &= (g == ref.astype(np.float32).astype(np.float64))
+    worst = float(np.max(err / bound)) if err.size else 0.0
+    return bool(ok.all()), worst, int(ok.size - int(ok.sum()))
+
+
+def verify_sample(w, A, B, C, gpu_results, row_ref, n_elements=4096, seed=12345):
+    """`gpu_results`: {path: flat C after one call on a fresh C}. Checks each
+    against the oracle rows the CPU baseline computed (row_ref: first rows of C)
+    and against n_elements seeded elements anywhere in C (the last row and
+    column among them)."""
+    import numpy as np
+
+    import oracle
+    ref_rows, mag_rows = row_ref
+    nrows = ref_rows.shape[0]
+    rng = np.random.default_rng(seed)
+    ri = rng.integers(0, w.M, n_elements)
+    ci = rng.integers(0, w.N, n_elements)
+    ri[:3] = [w.M - 1, w.M - 1, 0]
+    ci[:3] = [w.N - 1, 0, w.N - 1]
+    Cn = None if w.beta == 0 else C.numpy()
+    ref_el, mag_el = oracle.sgemm_elements(w.M, w.N, w.K, w.alpha, A.numpy(), w.LDA, B.numpy(),
+                                           w.LDB, w.beta, Cn, w.LDC, ri, ci)
+    exact = w.dist == "int3"
+    out = {}
+    for path, flat in gpu_results.items():
+        g = np.asarray(flat, dtype=np.float32)
+        rows = g[:nrows * w.LDC].reshape(nrows, w.LDC)[:, :w.N] if nrows else g[:0].reshape(0, w.N)
+        ok_r, worst_r, bad_r = check_against_reference(rows, ref_rows, mag_rows, exact)
+        ok_e, worst_e, bad_e = check_against_reference(g[ri * w.LDC + ci], ref_el, mag_el, exact)
+        out[path] = {"ok": ok_r and ok_e, "rows_checked": int(nrows),
+                     "elements_checked": int(n_elements), "mismatches": bad_r + bad_e,
+                     "worst_error_over_bound": round(max(worst_r, worst_e), 6),
+                     "bit_exact_required": exact}
+    return out
+
+
+def cpu_baseline(w, A, B, C, budget_s=10.0, gpu_results=None):
     """The oracle as it stands, on the host cores, over a growing row sample
-    until about budget_s of CPU work has been timed."""
+    until about budget_s of CPU work has been timed. With gpu_results
+    ({path: flat C from one call on a fresh C}), the rows it computed (plus a
+    sample of elements) also check those results: the `verification` entry."""
     threads = len(os.sched_getaffinity(0))
-    rows, spent, total_rows = max(1, threads), 0.0, 0
+    rows, spent, total_rows, row_ref = max(1, threads), 0.0, 0, None
     while True:
         rows = min(rows, w.M)
-        dt = oracle_rows_timing(w, A, B, C, rows, threads)
+        dt, ref = oracle_rows_timing(w, A, B, C, rows, threads, keep=True)
         if dt >= budget_s / 4 or rows == w.M:
-            spent, total_rows = dt, rows
+            spent, total_rows, row_ref = dt, rows, ref
             break
         rows = min(w.M, max(rows * 2, int(rows * (budget_s / 4) / max(dt, 1e-3))))
     value = gemm_flops(total_rows, w.N, w.K) / spent / 1e9
     # one core, on a few rows (about a second)
     one_rows = max(1, min(w.M, int(total_rows * 0.2 / max(threads, 1))))
     one_dt = oracle_rows_timing(w, A, B, C, one_rows, 1)
-    return {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "single_core_value": round(gemm_flops(one_rows, w.N, w.K) / one_dt / 1e9, 3),
-            "cpu_model": cpu_model(),
-            "sample": f"first {total_rows} of {w.M} rows of C ({w.N} columns, K={w.K}), "
-                      f"{spent:.2f} s, FP64 i-j-k loop, rows split over {threads} threads; "
-                      f"single core: first {one_rows} rows, {one_dt:.2f} s"}
+    out = {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+           "single_core_value": round(gemm_flops(one_rows, w.N, w.K) / one_dt / 1e9, 3),
+           "cpu_model": cpu_model(),
+           "sample": f"first {total_rows} of {w.M} rows of C ({w.N} columns, K={w.K}), "
+                     f"{spent:.2f} s, FP64 i-j-k loop, rows split over {threads} threads; "
+                     f"single core: first {one_rows} rows, {one_dt:.2f} s"}
+    if gpu_results:
+        out["verification"] = verify_sample(w, A, B, C, gpu_results, row_ref)
+    return out
 
 
 def cpu_model():
@@ -343,16 +534,39 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
-    def step():
+    def step(out=None):
         st = binding.sgemm(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(), w.LDB,
-                           w.beta, dC.data_ptr(), w.LDC, sh)
+                           w.beta, (dC if out is None else out).data_ptr(), w.LDC, sh)
         if st != 0:
             raise RuntimeError(f"sgemm: {binding.sgemm_status_string(st)}")
 
-    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
-    gpu_id = visible[local] if local < len(visible) else str(local)
-    sampler = ClockSampler(gpu_id) if rank == 0 else None
-    time.sleep(1.0 if sampler else 0.0)
+    def step3(out=None):
+        st3 = binding.sgemm_3xtf32(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA, dB.data_ptr(),
+                                   w.LDB, w.beta, (dC if out is None else out).data_ptr(), w.LDC,
+                                   sh)
+        if st3 != 0:
+            raise RuntimeError(f"sgemm_3xtf32: {binding.sgemm_status_string(st3)}")
+
+    # one call of each timed path on a fresh C, before any timing; the CPU
+    # baseline leg checks these results against the oracle
+    fresh = {}
+    if rank == 0 and args.cpu_baseline:
+        for path, fn in (("ffma", step), ("3xtf32", step3)):
+            if path == "3xtf32" and not args.tf32x3:
+                continue
+            out = C.to(dev)
+            fn(out)
+            torch.cuda.synchronize(dev)
+            fresh[path] = out.cpu().numpy()
+            del out
+
+    sampler = None
+    if rank == 0:
+        sampler = NvmlClockSampler(pci_bus_id=nvml_bus_id(props)).start()
+        if sampler.lib is None:
+            visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+            sampler = ClockSampler(visible[local] if local < len(visible) else str(local))
+            time.sleep(1.0)
 
     with nvtx_range("warmup"):
         for _ in range(args.warmup):
@@ -381,7 +595,8 @@ def run_ours(args, w):
     barrier(world)
     t_wall1 = time.time()
     total_s = start.elapsed_time(end) / 1e3
-    kern_s = sum(a.elapsed_time(b) for a, b in ev) / 1e3 / args.steps
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_s = sum(step_ms) / 1e3 / args.steps
     if sampler:
         sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
@@ -395,20 +610,19 @@ def run_ours(args, w):
     # ---- the opt-in tensor-core path on the same workload (reported apart) ---------
     tf32x3 = None
     if args.tf32x3:
-        def step3():
-            st3 = binding.sgemm_3xtf32(w.M, w.N, w.K, w.alpha, dA.data_ptr(), w.LDA,
-                                       dB.data_ptr(), w.LDB, w.beta, dC.data_ptr(), w.LDC, sh)
-            if st3 != 0:
-                raise RuntimeError(f"sgemm_3xtf32: {binding.sgemm_status_string(st3)}")
         for _ in range(args.warmup):
             step3()
         barrier(world)
         torch.cuda.synchronize(dev)
         s3, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev3 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
         with nvtx_range("tf32x3_steps"):
             s3.record(stream)
-            for _ in range(args.steps):
+            for i in range(args.steps):
+                ev3[i][0].record(stream)
                 step3()
+                ev3[i][1].record(stream)
             e3.record(stream)
             torch.cuda.synchronize(dev)
         t3 = max_over_ranks(s3.elapsed_time(e3) / 1e3, world)
@@ -417,6 +631,7 @@ def run_ours(args, w):
             raise RuntimeError(f"device status {st} detail {detail} after the 3xTF32 steps")
         v3 = aggregate(gemm_flops(w.M, w.N, w.K), args.steps, t3, world)
         tf32x3 = {"value": round(v3, 1), "unit": UNIT, "ms_per_step": round(t3 / args.steps * 1e3, 4),
+                  "step_ms": step_stats([a.elapsed_time(b) for a, b in ev3]),
                   "config": binding.sgemm_last_config(),
                   "note": "opt-in sgemm_3xtf32: split-operand TF32 on tcgen05, same FP32 tolerance; "
                           "includes its B-transpose pre-pass kernel"}
@@ -464,8 +679,9 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_max / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(w), parallelism=f"replicas{world}",
-                       tile_config=tile_config),
+        "config": workload_config(w),
+        "parallelism": f"replicas{world}", "tile_config": tile_config,
+        "step_ms": step_stats(step_ms),
         "pct_of_ffma_peak": round(100 * achieved_tf / peak_tf, 2),
         "pct_of_ffma_peak_at_sampled_clock": (round(100 * achieved_tf / ffma_peak_tflops(sms, sampled), 2)
                                               if sampled else None),
@@ -494,7 +710,17 @@ def run_ours(args, w):
                               "peak_from_bf16_estimate": round(est, 3) if est else None}
         line["tf32x3"] = tf32x3
     if args.cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, A, B, C, budget_s=args.cpu_budget)
+        cb = cpu_baseline(w, A, B, C, budget_s=args.cpu_budget, gpu_results=fresh)
+        ver = cb.pop("verification", None)
+        line["cpu_baseline"] = cb
+        line["verified"] = bool(ver) and all(v["ok"] for v in ver.values())
+        line["verification"] = dict(ver or {}, rule=TOLERANCE_RULE,
+                                    how="one call per path on a fresh C before any timing, "
+                                        "against the oracle rows the CPU baseline computed "
+                                        "and seeded single elements")
+    else:
+        line["verified"] = None
+        line["verification"] = {"skipped": "--no-cpu-baseline (the oracle runs in that leg)"}
     return line
 
 

@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_diag_wait_timeout": (I, [LL, P]),
                 "sgemm_set_wait_timeout_ns": (LL, [LL]),
                 "sgemm_noalloc": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
+                "sgemm_noalloc_poll_status": (I, [P, IP]),
                 "sgemm_choose_config": (I, [I, I, I, IP]),
                 "sgemm_3xtf32": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
                 "sgemm_ex": (I, [I, I, I, I, I, F, P, I, P, I, F, P, I, P]),
@@ -258,6 +259,14 @@ def sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> 
     the kernel's scratch comes from a fixed buffer inside the library.
     Returns the status code."""
     return lib().sgemm_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def sgemm_noalloc_poll_status(stream=None):
+    """(status, device detail code) of the sgemm_noalloc calls on this device
+    since the last poll; synchronises `stream` first."""
+    detail = ctypes.c_int(0)
+    st = lib().sgemm_noalloc_poll_status(stream, ctypes.byref(detail))
+    return st, detail.value
 
 
 def sgemm_ladder(kernel, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

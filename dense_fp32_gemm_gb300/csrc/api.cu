@@ -284,8 +284,8 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
 
   const int occ = di->occupancy[id];
   if (occ < 1) return SGEMM_ERR_LAUNCH;
-  const int tiles_m = (M + S.BM - 1) / S.BM, tiles_n = (N + S.BN - 1) / S.BN;
-  const int kiters = (K + S.BK - 1) / S.BK;
+  const int tiles_m = ceil_div_nn(M, S.BM), tiles_n = ceil_div_nn(N, S.BN);
+  const int kiters = ceil_div_nn(K, S.BK);
   const long long total_tiles = (long long)tiles_m * tiles_n * batch;
   if (total_tiles > 0x7fffffffLL) return SGEMM_ERR_INVALID_DIM;
   Schedule sched = make_schedule(tiles_m, tiles_n, kiters, di->sms * occ, kGroupM, kMinSplitUnits,
@@ -546,8 +546,10 @@ SGEMM_API int sgemm_schedule_query(int M, int N, int K, int id, int capacity, in
   if (id < 0 || id >= kNumConfigs || capacity < 1 || out == nullptr)
     return SGEMM_ERR_INVALID_VALUE;
   const TileShape& S = kConfigs[id]->shape;
-  const Schedule s = make_schedule((M + S.BM - 1) / S.BM, (N + S.BN - 1) / S.BN,
-                                   (K + S.BK - 1) / S.BK, capacity, kGroupM, kMinSplitUnits);
+  if ((long long)ceil_div_nn(M, S.BM) * ceil_div_nn(N, S.BN) > 0x7fffffffLL)
+    return SGEMM_ERR_INVALID_DIM;
+  const Schedule s = make_schedule(ceil_div_nn(M, S.BM), ceil_div_nn(N, S.BN),
+                                   ceil_div_nn(K, S.BK), capacity, kGroupM, kMinSplitUnits);
   const int v[8] = {s.tiles_m, s.tiles_n, s.kiters, s.grid, s.dp_tiles, s.sk_q, s.sk_r, s.group_m};
   for (int i = 0; i < 8; ++i) out[i] = v[i];
   return SGEMM_OK;

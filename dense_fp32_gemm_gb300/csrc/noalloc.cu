@@ -20,18 +20,20 @@
 //     schedule needs more returns SGEMM_ERR_NOALLOC_CAPACITY and launches
 //     nothing;
 //   * all calls share the one array and it keeps the last call's contents.
-//     The status word is cleared at the start of every call; the flags are
-//     matched against a per-device call counter, so stale flags are never
-//     mistaken for fresh ones (they are cleared whenever the counter wraps);
-//     partial tiles are always written before they are read. Calls that
-//     overlap on the GPU (two streams, or two host threads) race on the array;
+//     The flags are matched against a per-device call counter, so stale flags
+//     are never mistaken for fresh ones (they are cleared whenever the counter
+//     wraps, and by a poll that reports a timeout); partial tiles are always
+//     written before they are read. Calls that overlap on the GPU (two
+//     streams, or two host threads) race on the array;
 //   * the first call on a device performs its set-up: it looks up the
 //     array's device address (cudaGetSymbolAddress, with that device current)
 //     and sets the kernels' shared-memory attributes. Make that first call
 //     before any stream capture;
-//   * a kernel that gives up on a bounded wait records its code in the
-//     array's status word, which the next call clears; sgemm_poll_device_status
-//     does not see it.
+//   * every wait inside the kernel is bounded by the library's wait limit
+//     (sgemm_set_wait_timeout_ns); a kernel that gives up records its code in
+//     the array's status word, which stays set until sgemm_noalloc_poll_status
+//     reads and clears it (that poll also clears the flags, which an aborted
+//     call can leave published).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -50,6 +52,9 @@
 #define SGEMM_API extern "C" __attribute__((visibility("default")))
 
 namespace sgemm_gb300 {
+
+// Provided by api.cu.
+long long library_wait_timeout_ns();
 
 // The kernel for very small problems (tiny.cu); it needs no scratch.
 bool tiny_wanted(int M, int N, int K);
@@ -205,6 +210,9 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   const int id = choose_config(M, N, K);
   const ConfigEntry& cfg = *kNoAllocConfigs[id];
   const TileShape& S = cfg.shape;
+  // the schedule numbers tiles with 32-bit integers (the same limit as sgemm())
+  const int tiles_m = ceil_div_nn(M, S.BM), tiles_n = ceil_div_nn(N, S.BN);
+  if ((long long)tiles_m * tiles_n > 0x7fffffffLL) return SGEMM_ERR_INVALID_DIM;
 
   bool tma = ((reinterpret_cast<uintptr_t>(B) & 15u) == 0) && ((ldb & 3) == 0);
   CUtensorMap map_a, map_b;
@@ -229,9 +237,8 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
 
   const int occ = d->occupancy[id];
   if (occ < 1) return SGEMM_ERR_LAUNCH;
-  const Schedule sched =
-      make_schedule((M + S.BM - 1) / S.BM, (N + S.BN - 1) / S.BN, (K + S.BK - 1) / S.BK,
-                    d->sms * occ, kNaGroupM, kNaMinSplitUnits);
+  const Schedule sched = make_schedule(tiles_m, tiles_n, ceil_div_nn(K, S.BK),
+                                       d->sms * occ, kNaGroupM, kNaMinSplitUnits);
   const bool split = sched.dp_tiles < sched.tiles;
   const size_t partial_bytes = split ? (size_t)sched.grid * S.BM * S.BN * 4 : 0;
   if ((size_t)sched.grid > kNoAllocMaxFlags ||
@@ -241,9 +248,9 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   int* status = reinterpret_cast<int*>(d->base);
   uint32_t* flags = reinterpret_cast<uint32_t*>(d->base + kNoAllocStatusBytes);
   float* partials = reinterpret_cast<float*>(d->base + kNoAllocHeaderBytes);
-  // the status word starts every call at zero; the flags only on a wrap of
-  // the call counter (a flag is fresh when it equals this call's number)
-  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  // the flags are cleared on a wrap of the call counter (a flag is fresh when
+  // it equals this call's number); the status word keeps the first recorded
+  // code until sgemm_noalloc_poll_status clears it
   if (++d->epoch == 0) {
     d->epoch = 1;
     if (cudaMemsetAsync(flags, 0, kNoAllocMaxFlags * 4, stream) != cudaSuccess)
@@ -271,11 +278,43 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   p.status = status;
   p.epoch = d->epoch;
   p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && ((ldc & 3) == 0);
-  p.timeout_ns = 4000000000LL;
+  p.timeout_ns = library_wait_timeout_ns();
   if (cfg.launch(kARow, tma ? kBRowTma : kBRowCp, sched.grid, p, &map_a, &map_b, stream) !=
       cudaSuccess) {
     cudaGetLastError();
     return SGEMM_ERR_LAUNCH;
   }
   return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_noalloc_poll_status(void* stream_, int* detail) {
+  if (detail) *detail = 0;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  if (dev < 0 || dev >= kNoAllocMaxDevices || !g_na_devices[dev].ready) return SGEMM_OK;
+  NoAllocDevice& d = g_na_devices[dev];
+  int code = 0;
+  // plain synchronous copies to and from the array: nothing is allocated
+  if (cudaMemcpy(&code, d.base, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  if (code == 0) return SGEMM_OK;
+  // an aborted call can leave flags published that no owner consumed; a
+  // replayed graph reuses its call number, so clear them
+  if (cudaMemset(d.base, 0, kNoAllocHeaderBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  if (detail) *detail = code;
+  return SGEMM_ERR_DEVICE_TIMEOUT;
 }

@@ -55,6 +55,8 @@ struct Piece {
 };
 
 SG_HD int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+// ceil(a / b) for 0 <= a <= INT_MAX and b >= 1, without overflow near INT_MAX.
+SG_HD int ceil_div_nn(int a, int b) { return (int)(((long long)a + b - 1) / b); }
 
 // Tile index -> (tile row, tile column) in grouped raster order.
 SG_HD void tile_coords(const Schedule& s, int t, int& tm, int& tn) {

@@ -175,20 +175,24 @@ __global__ void pack_a_kernel(int M, int K, const float* __restrict__ A, long lo
 }
 
 // B (K x N, ldb) -> B^T (N x K, ldw), through 32 x 32 shared-memory tiles so
-// that both the reads and the writes are coalesced.
+// that both the reads and the writes are coalesced. Tile columns over
+// blockIdx.x, tile rows over blockIdx.y strided by gridDim.y (any K).
 __global__ void transpose_b_kernel(int K, int N, const float* __restrict__ B, long long ldb,
                                    float* __restrict__ bt, long long ldw) {
   __shared__ float tile[32][33];
-  const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+  const long long n0 = (long long)blockIdx.x * 32;
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
-  for (int j = 0; j < 32; j += 8) {
-    const int k = k0 + ty + j, n = n0 + tx;
-    tile[ty + j][tx] = (k < K && n < N) ? B[(long long)k * ldb + n] : 0.f;
-  }
-  __syncthreads();
-  for (int j = 0; j < 32; j += 8) {
-    const int n = n0 + ty + j, k = k0 + tx;
-    if (n < N && k < K) bt[(long long)n * ldw + k] = tile[tx][ty + j];
+  for (long long k0 = (long long)blockIdx.y * 32; k0 < K; k0 += (long long)gridDim.y * 32) {
+    for (int j = 0; j < 32; j += 8) {
+      const long long k = k0 + ty + j, n = n0 + tx;
+      tile[ty + j][tx] = (k < K && n < N) ? B[k * ldb + n] : 0.f;
+    }
+    __syncthreads();
+    for (int j = 0; j < 32; j += 8) {
+      const long long n = n0 + ty + j, k = k0 + tx;
+      if (n < N && k < K) bt[n * ldw + k] = tile[tx][ty + j];
+    }
+    __syncthreads();  // the tile is rewritten by the next row of tiles
   }
 }
 
@@ -666,13 +670,13 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   // schedule: whole tiles, then the last one to two waves split along K. In
   // the pair form a schedule unit is two vertically adjacent tiles (a tile
   // row pair), handed to one cluster.
-  const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+  const int tiles_m = ceil_div_nn(M, BM), tiles_n = ceil_div_nn(N, BN);
   // the k-slice width (see Slice). The two-SM form always takes 32: its
   // stages halve the per-stage hand-offs between the CTAs of a pair
   // (measured at 4096^3: 265 against 158 TFLOP/s with 16).
   auto slice_width = [K](int f) { return (f == kTwoSmPair || K < 1024) ? 32 : 16; };
   pl.bk = slice_width(pl.form);
-  pl.kiters = (K + pl.bk - 1) / pl.bk;
+  pl.kiters = ceil_div_nn(K, pl.bk);
   if (pl.form != kSingle) {
     // groups of 8 tile-row pairs in the raster (measured at 8192^3: 309 against
     // 305 TFLOP/s with 4, 298 with 2; 16 the same as 8)
@@ -684,7 +688,7 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   }
   if (pl.form == kSingle) {
     pl.bk = slice_width(pl.form);
-    pl.kiters = (K + pl.bk - 1) / pl.bk;
+    pl.kiters = ceil_div_nn(K, pl.bk);
     // at least 64 of K per CTA in a split
     pl.sched = make_schedule(tiles_m, tiles_n, pl.kiters, sms, 8, 64 / pl.bk);
   }
@@ -750,6 +754,9 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     x3::scale_c_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
   }
+  // the schedule numbers tiles with 32-bit integers (the same limit as sgemm())
+  if ((long long)ceil_div_nn(M, x3::BM) * ceil_div_nn(N, x3::BN) > 0x7fffffffLL)
+    return SGEMM_ERR_INVALID_DIM;
 
   int pairs = 0;
   {
@@ -821,7 +828,9 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
 
   // 1. B^T (and, when needed, an aligned copy of A)
   {
-    dim3 grid((N + 31) / 32, (K + 31) / 32), block(32, 8);
+    const int ktiles = ceil_div_nn(K, 32);
+    dim3 grid((unsigned)ceil_div_nn(N, 32), (unsigned)(ktiles < 65535 ? ktiles : 65535)),
+        block(32, 8);
     x3::transpose_b_kernel<<<grid, block, 0, stream>>>(K, N, B, ldb, bt, Kp);
     if (!a_direct) {
       const int bx = (K + 255) / 256 < 8 ? (K + 255) / 256 : 8;
@@ -893,6 +902,8 @@ SGEMM_API int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sm
   if ((form != SGEMM_X3_SINGLE && form != SGEMM_X3_PAIR) || pairs < 0 || sms < 1 ||
       out == nullptr)
     return SGEMM_ERR_INVALID_VALUE;
+  if ((long long)ceil_div_nn(M, x3::BM) * ceil_div_nn(N, x3::BN) > 0x7fffffffLL)
+    return SGEMM_ERR_INVALID_DIM;
   const x3::Plan pl = x3::make_plan(M, N, K, form, pairs, sms);
   out[0] = pl.form;
   out[1] = pl.bk;

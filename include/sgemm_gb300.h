@@ -83,6 +83,12 @@ typedef enum {
  * M * N * K <= 2^25 run a latency-first kernel (one CTA per 32 x 32 tile, no
  * K-split) unless a tile configuration is forced; larger ones the persistent
  * kernel with the tuned configuration of their shape class.
+ * Pages: the result is the one every kernel of "Shared Memory Tiling" (kernel
+ * listing, final store), "Vectorized Memory Access: 128-bit Loads and Stores"
+ * and "Warp Tiling: A Third Level of Tiling" (section "The Kernel",
+ * epilogues) computes. The pages are silent on leading dimensions, shapes that
+ * are not tile multiples, alignment, and the beta == 0 / alpha == 0 / K == 0
+ * cases; the rules above are the plain BLAS reading of those points.
  */
 int sgemm(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
           float beta, float* C, int ldc, void* stream);
@@ -114,7 +120,8 @@ int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int lda, cons
  * pairs and the problem has at least two waves of whole tile pairs, else
  * single CTAs. Both give the same results within the tolerance (bit-identical
  * on integer inputs). Returns the previous setting, or
- * SGEMM_ERR_INVALID_VALUE (nothing changed) for another value.
+ * SGEMM_ERR_INVALID_VALUE (nothing changed) for another value. The pages are
+ * silent (no tensor-core kernel).
  */
 #define SGEMM_X3_SINGLE 1
 #define SGEMM_X3_PAIR 2
@@ -130,6 +137,7 @@ int sgemm_3xtf32_set_kernel_form(int form);
  * would be split along K. Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM unless
  * M, N, K >= 1 (only such problems launch the GEMM kernel), or
  * SGEMM_ERR_INVALID_VALUE for another form, pairs < 0, sms < 1 or a NULL out.
+ * The pages are silent (no tensor-core kernel, one CTA per tile).
  */
 int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sms, int* out);
 
@@ -143,6 +151,8 @@ int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sms, int* ou
  * row-major A. Column-major callers: a column-major M x N result is the
  * row-major N x M result of op(B)^T op(A)^T, i.e. call with the operands and
  * M, N swapped. Otherwise as sgemm(); SGEMM_ERR_INVALID_VALUE for another op.
+ * The pages compute row-major A * B only; transposed operands are the BLAS
+ * generalisation they never reach (silent).
  */
 int sgemm_ex(int opA, int opB, int M, int N, int K, float alpha, const float* A, int lda,
              const float* B, int ldb, float beta, float* C, int ldc, void* stream);
@@ -154,6 +164,7 @@ int sgemm_ex(int opA, int opB, int M, int N, int K, float alpha, const float* A,
  * which is only valid for A and B). One launch covers every product: the
  * batch index is the outermost tile coordinate of the persistent schedule.
  * C_i must not overlap each other or any A_j, B_j. batch == 0 does nothing.
+ * The pages are silent (one product per launch).
  */
 int sgemm_strided_batched(int opA, int opB, int M, int N, int K, float alpha, const float* A,
                           int lda, long long strideA, const float* B, int ldb, long long strideB,
@@ -172,6 +183,7 @@ int sgemm_strided_batched(int opA, int opB, int M, int N, int K, float alpha, co
  * valid until then. Device buffers, two copy streams and their events are
  * owned by the library per (device, stream) and reused by later calls (freed
  * by sgemm_shutdown). Same argument checks and status codes as sgemm().
+ * The pages are silent: they time device-resident operands only.
  */
 int sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
                float beta, float* C, int ldc, void* stream);
@@ -185,17 +197,21 @@ int sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, const 
  * 512 * panels). Widths are rounded up to multiples of 32; at most 9 chunks.
  * The result does not depend on the setting beyond the order of the sum
  * over k. Returns SGEMM_ERR_INVALID_VALUE (nothing changed) for a negative
- * value or more than 8 panels.
+ * value or more than 8 panels. The pages are silent.
  */
 int sgemm_host_set_pipeline(int first, int mid, int last, int panels);
 
-/* Human-readable text for a status code (static storage, never NULL). */
+/* Human-readable text for a status code (static storage, never NULL). The
+ * pages are silent: their kernels return no status. */
 const char* sgemm_status_string(int status);
 
 /*
  * Name of the tile configuration and schedule the calling thread's last
  * sgemm() used, copied into buf (at most len bytes, NUL-terminated).
  * Returns SGEMM_OK, or SGEMM_ERR_INVALID_VALUE if buf is NULL or len < 1.
+ * The pages name the configuration beside every measurement ("Autotuning:
+ * Searching the Tile-Shape Space", section "What The Sweep Found"); this is
+ * that name for the library's own choice.
  */
 int sgemm_last_config(char* buf, int len);
 
@@ -207,12 +223,15 @@ int sgemm_last_config(char* buf, int len);
  * split partial, 4 = CTA rendezvous, 5 = the two CTAs of a two-SM pair of
  * sgemm_3xtf32 got different tensor-memory columns; none of them is a device
  * fault, and the context stays usable). SGEMM_ERR_LAUNCH if synchronising
- * fails.
+ * fails. `detail` extends the survey's one-argument form of this call: the
+ * status alone cannot say which wait gave up. The pages are silent (their
+ * kernels have no bounded waits and report nothing).
  */
 int sgemm_poll_device_status(void* stream, int* detail);
 
 /* Frees every workspace, device buffer, stream and event the library
- * allocated (after synchronising the device). Later calls allocate again. */
+ * allocated (after synchronising the device). Later calls allocate again.
+ * The pages are silent (their kernels allocate nothing). */
 void sgemm_shutdown(void);
 
 /*
@@ -222,13 +241,18 @@ void sgemm_shutdown(void);
  * {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES, MINB, KU, ORDER} in
  * params[13] (KU: k-steps per unrolled chunk; ORDER: 0 row-by-row FFMA, 1 zig-zag
  * FFMA, 2 paired FMA, 3 paired FMA column by column).
+ * Pages: the tuple of "Autotuning: Searching the Tile-Shape Space", section
+ * "Mechanics" (the kernel's template parameters), plus this kernel's own
+ * pipeline depth, residency, unroll and FMA order.
  */
 int sgemm_config_count(void);
 int sgemm_config_info(int id, char* name, int len, int* params);
 
 /*
  * Forces every later sgemm() on this process to use configuration `id`
- * (-1 restores the automatic per-shape choice). For tuning and tests.
+ * (-1 restores the automatic per-shape choice). For tuning and tests; the
+ * sweep of "Autotuning: Searching the Tile-Shape Space" ("Mechanics") times
+ * one configuration at a time in the same way.
  */
 int sgemm_force_config(int id);
 
@@ -236,6 +260,7 @@ int sgemm_force_config(int id);
  * 1 when tile configuration `id` is built for every operand layout (op(A),
  * op(B) in {N, T}; sgemm_ex and sgemm_strided_batched can use it), 0 when
  * only for row-major A and B, SGEMM_ERR_INVALID_VALUE for an unknown id.
+ * The pages are silent (row-major operands only).
  */
 int sgemm_config_layouts(int id);
 
@@ -246,6 +271,10 @@ int sgemm_config_layouts(int id);
  * 0 square-large, 1 square-small, 2 K-dominant, 3 N <= 96, 4 M <= 96,
  * 5 tiny (at most 2^28 multiply-adds).
  * Returns the configuration id or SGEMM_ERR_INVALID_DIM. Host only.
+ * Pages: "Autotuning: Searching the Tile-Shape Space" picks one configuration
+ * by measurement for one shape ("What The Sweep Found") and notes that the
+ * winner depends on the shape ("What Could Be Improved"); this repeats the
+ * search per shape class.
  */
 int sgemm_choose_config(int M, int N, int K, int* shape_class);
 
@@ -255,6 +284,10 @@ int sgemm_choose_config(int M, int N, int K, int* shape_class);
  * rule it breaks. params = {BM, BN, BK, WM, WN, WNITER, TM, TN, NT, STAGES,
  * MINB, KU, ORDER}. derived (if not NULL) receives {WMITER, WSUBM, WSUBN, accumulators
  * per thread, shared bytes per CTA} when the tuple is legal.
+ * Pages: "Autotuning: Searching the Tile-Shape Space", sections "Most
+ * Configurations Are Not Wrong By A Little" (the kernel's unstated
+ * assumptions) and "Mechanics" (a compile-time legality gate); the rules here
+ * are this kernel's own assumptions.
  */
 int sgemm_cfg_check(const int* params, int* derived);
 
@@ -263,6 +296,8 @@ int sgemm_cfg_check(const int* params, int* derived);
  * configuration `id` on `capacity` resident CTAs (host arithmetic only, no
  * device needed). out = {tiles_m, tiles_n, kiters, grid, dp_tiles, sk_q,
  * sk_r, group_m}. Returns SGEMM_OK or an argument error.
+ * The pages launch one CTA per C tile ("Shared Memory Tiling", kernel launch
+ * grid); the persistent schedule is this library's (silent on the pages).
  */
 int sgemm_schedule_query(int M, int N, int K, int id, int capacity, int* out);
 
@@ -270,7 +305,8 @@ int sgemm_schedule_query(int M, int N, int K, int id, int capacity, int* out);
  * Piece `i` of CTA `b` under the schedule {tiles_m, tiles_n, kiters, grid,
  * dp_tiles, sk_q, sk_r, group_m} (as returned above): out = {tile, kb, ke,
  * tile_m, tile_n, contributors, is_partial}. Returns the number of pieces of
- * CTA b, or a negative status. Host arithmetic only.
+ * CTA b, or a negative status. Host arithmetic only. Pages: silent (see
+ * sgemm_schedule_query).
  */
 int sgemm_schedule_piece(const int* sched, int b, int i, int* out);
 
@@ -279,12 +315,13 @@ int sgemm_schedule_piece(const int* sched, int b, int i, int* out);
  * ever arrives on, with a limit of timeout_ns, through the same bounded wait
  * the GEMM kernels use. The wait must run out and record device code 1; read
  * it with sgemm_poll_device_status(). Nothing faults and nothing hangs.
+ * The pages are silent.
  */
 int sgemm_diag_wait_timeout(long long timeout_ns, void* stream);
 
 /* Upper bound, in nanoseconds, of every wait inside the kernels (default
  * 4e9). Values < 1000 are rejected. Returns the previous value or a negative
- * status. */
+ * status. The pages are silent. */
 long long sgemm_set_wait_timeout_ns(long long ns);
 
 /*
@@ -295,7 +332,7 @@ long long sgemm_set_wait_timeout_ns(long long ns);
  * (about 6 ms at iters = 20000 on GB300). Synchronous. The 3xTF32 path's
  * roofline divides this by three. Returns SGEMM_ERR_INVALID_VALUE for iters
  * < 1 or a NULL result pointer, SGEMM_ERR_DEVICE_TIMEOUT if the MMAs did not
- * complete within 4 s.
+ * complete within 4 s. The pages are silent (no tensor-core kernel).
  */
 int sgemm_diag_tf32_mma_rate(int iters, double* tflops);
 
@@ -305,7 +342,7 @@ int sgemm_diag_tf32_mma_rate(int iters, double* tflops);
  * CTA issues `iters` x 4 tcgen05.mma.cta_group::2.kind::tf32 of M 256 (128
  * rows per CTA), N 256 (half of B in each CTA), K 8. The rate counts the
  * multiply-adds of all SMs taking part. Same arguments, errors and duration
- * as sgemm_diag_tf32_mma_rate.
+ * as sgemm_diag_tf32_mma_rate. The pages are silent.
  */
 int sgemm_diag_tf32_pair_mma_rate(int iters, double* tflops);
 
@@ -325,14 +362,29 @@ int sgemm_diag_tf32_pair_mma_rate(int iters, double* tflops);
  * capture. A problem whose schedule needs more scratch than the array holds
  * returns SGEMM_ERR_NOALLOC_CAPACITY and launches nothing (on a 152-SM GB300
  * every problem fits). All calls share the array: calls that overlap on the
- * GPU (other streams, other host threads) race and must not be issued. The
- * device status of these calls is kept in the array and cleared by the next
- * call; sgemm_poll_device_status() does not report it. The tile configuration
- * is always the automatic choice (sgemm_force_config() does not apply), and
- * problems with M * N * K <= 2^25 run the same tiny-problem kernel as sgemm().
+ * GPU (other streams, other host threads) race and must not be issued. Every
+ * wait inside the kernel is bounded by the library's wait limit
+ * (sgemm_set_wait_timeout_ns). A kernel that gives up records its code in the
+ * array, where it stays until sgemm_noalloc_poll_status() reads it
+ * (sgemm_poll_device_status() reports only the per-stream workspaces). The
+ * tile configuration is always the automatic choice (sgemm_force_config()
+ * does not apply), and problems with M * N * K <= 2^25 run the same
+ * tiny-problem kernel as sgemm().
  */
 int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
                   int ldb, float beta, float* C, int ldc, void* stream);
+
+/*
+ * Waits for `stream`, then reports and clears the device status that
+ * sgemm_noalloc calls on the current device recorded in the library's fixed
+ * array: SGEMM_OK, or SGEMM_ERR_DEVICE_TIMEOUT with *detail (if not NULL)
+ * set to the code (the same codes as sgemm_poll_device_status). After a
+ * timeout it also clears the array's split-K flags, which an aborted call can
+ * leave published. Allocates nothing. SGEMM_OK when sgemm_noalloc has not
+ * run on this device; SGEMM_ERR_LAUNCH if synchronising or a copy fails.
+ * The pages have no counterpart (they report no device-side errors).
+ */
+int sgemm_noalloc_poll_status(void* stream, int* detail);
 
 /*
  * Three kernels of the pages' series, rebuilt for this GPU to measure what

@@ -85,5 +85,28 @@ def test_noalloc_argument_errors():
     assert binding.sgemm_noalloc(-1, 4, 4, 1.0, p, 4, p, 4, 0.0, p, 4, None) == binding.SGEMM_ERR_INVALID_DIM
     assert binding.sgemm_noalloc(4, 4, 4, 1.0, p, 3, p, 4, 0.0, p, 4, None) == binding.SGEMM_ERR_INVALID_LD
     assert binding.sgemm_noalloc(4, 4, 4, 1.0, p, 4, p, 4, 0.0, 0, 4, None) == binding.SGEMM_ERR_NULL_PTR
+    # more C tiles than the 32-bit schedule numbers: refused on the host, as by
+    # sgemm() (no operand is touched; the sizes only have to be consistent)
+    big = 2**31 - 1
+    assert binding.sgemm_noalloc(big, big, 1, 1.0, p, 1, p, big, 0.0, p, big, None) == binding.SGEMM_ERR_INVALID_DIM
+    assert binding.sgemm(big, big, 1, 1.0, p, 1, p, big, 0.0, p, big, None) == binding.SGEMM_ERR_INVALID_DIM
     torch.cuda.synchronize()
     assert torch.all(C == 5.0)
+
+
+def test_noalloc_honours_the_wait_limit_and_reports_status():
+    # a short (20 ms) limit on every wait still lets a split-K problem finish
+    # normally, twice in a row, with the same bits as sgemm(); the status the
+    # calls left in the fixed array reads clean
+    w = SPLIT
+    A, B, C = make_inputs(w)
+    dA, dB = A.to("cuda"), B.to("cuda")
+    ref = _call(binding.sgemm, w, dA, dB, C)
+    s = torch.cuda.current_stream().cuda_stream
+    prev = binding.sgemm_set_wait_timeout_ns(20_000_000)
+    try:
+        for _ in range(2):
+            assert np.array_equal(_call(binding.sgemm_noalloc, w, dA, dB, C), ref)
+        assert binding.sgemm_noalloc_poll_status(s) == (0, 0)
+    finally:
+        binding.sgemm_set_wait_timeout_ns(prev)
