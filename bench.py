@@ -104,7 +104,7 @@ def tf32x3_roof(binding, peaks, pair=False):
 # The sources that define the FFMA kernel the bench times and how it is
 # configured (the other entry points and the C-ABI dispatch are left out).
 FFMA_KERNEL_SOURCES = ("ffma_sgemm.cuh", "ptx.cuh", "schedule.hpp", "tile_config.hpp",
-                       "configs.hpp", "launch.cuh", "dispatch.hpp", "tuned_table.inc", "cfg_*.cu")
+                       "configs.hpp", "configs.inc", "launch.cuh", "dispatch.hpp", "tuned_table.inc")
 
 
 def kernel_source_hash():

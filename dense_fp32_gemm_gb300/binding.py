@@ -41,7 +41,9 @@ class SgemmError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The library to load: SGEMM_GB300_LIB if set (the tuner's candidate
+    build), else the in-tree product library."""
+    return os.environ.get("SGEMM_GB300_LIB") or _build.LIB_PATH
 
 
 def lib() -> ctypes.CDLL:
@@ -69,6 +71,9 @@ def lib() -> ctypes.CDLL:
                 "sgemm_cfg_check": (I, [IP, IP]),
                 "sgemm_schedule_query": (I, [I, I, I, I, I, IP]),
                 "sgemm_schedule_piece": (I, [IP, I, I, IP]),
+                "sgemm_schedule_plan": (I, [I, I, I, I, I, I, I, IP, IP]),
+                "sgemm_force_schedule": (I, [IP]),
+                "sgemm_choose_policy": (I, [I, I, I, IP]),
                 "sgemm_diag_wait_timeout": (I, [LL, P]),
                 "sgemm_set_wait_timeout_ns": (LL, [LL]),
                 "sgemm_noalloc": (I, [I, I, I, F, P, I, P, I, F, P, I, P]),
@@ -200,7 +205,8 @@ def sgemm_force_config(cid: int) -> int:
     return lib().sgemm_force_config(cid)
 
 
-SHAPE_CLASSES = ("square_large", "square_small", "k_dominant", "skinny_n", "skinny_m", "tiny")
+SHAPE_CLASSES = ("square_large", "square_small", "k_dominant", "skinny_n", "skinny_m", "tiny",
+                 "square_mid")
 
 
 def sgemm_choose_config(M, N, K):
@@ -234,6 +240,33 @@ def sgemm_schedule_query(M, N, K, cid, capacity):
     if st != SGEMM_OK:
         raise SgemmError(st, "sgemm_schedule_query")
     return dict(zip(SCHED_FIELDS, list(out)))
+
+
+SCHED_HYBRID, SCHED_HYBRID_TAIL, SCHED_DATA_PARALLEL, SCHED_STREAM_K, SCHED_SPLIT_K = 0, 1, 2, 3, 4
+SCHED_MODES = (SCHED_HYBRID, SCHED_HYBRID_TAIL, SCHED_DATA_PARALLEL, SCHED_STREAM_K, SCHED_SPLIT_K)
+
+
+def sgemm_schedule_plan(M, N, K, BM, BN, BK, capacity, policy):
+    """The schedule for BM x BN x BK tiles under `policy` = (mode, group_m,
+    min_units, splits), host arithmetic only; raises on an argument error."""
+    out = _ints(8)
+    st = lib().sgemm_schedule_plan(M, N, K, BM, BN, BK, capacity, _ints(4, policy), out)
+    if st != SGEMM_OK:
+        raise SgemmError(st, "sgemm_schedule_plan")
+    return dict(zip(SCHED_FIELDS, list(out)))
+
+
+def sgemm_force_schedule(policy=None) -> int:
+    """Force (mode, group_m, min_units, splits) on later calls; None restores
+    the tuned per-class policy. Returns the status code."""
+    return lib().sgemm_force_schedule(None if policy is None else _ints(4, policy))
+
+
+def sgemm_choose_policy(M, N, K):
+    """(status, (mode, group_m, min_units, splits)) that sgemm() takes by itself."""
+    out = _ints(4)
+    st = lib().sgemm_choose_policy(M, N, K, out)
+    return st, tuple(out)
 
 
 def sgemm_schedule_piece(sched: dict, b: int, i: int):

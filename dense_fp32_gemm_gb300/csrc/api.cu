@@ -40,12 +40,11 @@ const ConfigEntry* const kConfigs[] = {SGEMM_GB300_CONFIGS(SGEMM_GB300_ENTRY_PTR
 constexpr int kNumConfigs = sizeof(kConfigs) / sizeof(kConfigs[0]);
 static_assert(kNumConfigIds == kNumConfigs, "config ids");
 
-// Raster group height (tiles) and the fewest k-slices worth splitting off.
-constexpr int kGroupM = 8;
-constexpr int kMinSplitUnits = 4;
-
 std::mutex g_mutex;
 std::atomic<int> g_forced{-1};
+// A schedule policy forced for every later call (tuner, tests); mode < 0:
+// the tuned policy of the problem's shape class. Guarded by g_mutex.
+SchedPolicy g_forced_policy{-1, 8, 4, 1};
 std::atomic<long long> g_timeout_ns{4000000000LL};
 thread_local char g_last_config[192] = "none";
 
@@ -253,9 +252,10 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
   }
   if (id < 0 || id >= kNumConfigs || (!row_major && !kConfigs[id]->all_layouts))
     id = choose_config(M, N, K);
-  // transposed operands need a configuration built for them (the tuner only
-  // picks such configurations; this guards a table written by hand)
-  if (!row_major && !kConfigs[id]->all_layouts) id = kIdWideBk32F2Ku16;
+  const SchedPolicy policy =
+      g_forced_policy.mode >= 0 ? g_forced_policy : choose_policy(M, N, K);
+  // transposed operands need a configuration built for them
+  if (!row_major && !kConfigs[id]->all_layouts) id = kFallbackConfigId;
   const ConfigEntry& cfg = *kConfigs[id];
   const TileShape& S = cfg.shape;
 
@@ -288,8 +288,7 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
   const int kiters = ceil_div_nn(K, S.BK);
   const long long total_tiles = (long long)tiles_m * tiles_n * batch;
   if (total_tiles > 0x7fffffffLL) return SGEMM_ERR_INVALID_DIM;
-  Schedule sched = make_schedule(tiles_m, tiles_n, kiters, di->sms * occ, kGroupM, kMinSplitUnits,
-                                 batch);
+  Schedule sched = make_schedule(tiles_m, tiles_n, kiters, di->sms * occ, policy, batch);
 
   const bool split = sched.dp_tiles < sched.tiles;
   Workspace* ws = nullptr;
@@ -328,9 +327,11 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
   }
   static const char* const kAName[] = {"a=rowT", "a=tma", "a=cp"};
   static const char* const kBName[] = {"b=tma", "b=cp", "b=colT"};
-  snprintf(g_last_config, sizeof(g_last_config), "%s %s %s grid=%d dp=%d split=%d kiters=%d%s",
-           cfg.name, kAName[al], kBName[bl], sched.grid, sched.dp_tiles,
-           sched.tiles - sched.dp_tiles, sched.kiters, batch > 1 ? " batched" : "");
+  snprintf(g_last_config, sizeof(g_last_config),
+           "%s %s %s grid=%d dp=%d split=%d kiters=%d sched=%d/g%d/u%d/s%d%s", cfg.name,
+           kAName[al], kBName[bl], sched.grid, sched.dp_tiles, sched.tiles - sched.dp_tiles,
+           sched.kiters, policy.mode, sched.group_m, policy.min_units, policy.splits,
+           batch > 1 ? " batched" : "");
   return SGEMM_OK;
 }
 
@@ -541,17 +542,62 @@ SGEMM_API int sgemm_cfg_check(const int* params, int* derived) {
   return rule;
 }
 
+namespace {
+int schedule_out(int M, int N, int K, int BM, int BN, int BK, int capacity,
+                 const SchedPolicy& pol, int* out) {
+  if ((long long)ceil_div_nn(M, BM) * ceil_div_nn(N, BN) > 0x7fffffffLL)
+    return SGEMM_ERR_INVALID_DIM;
+  const Schedule s = make_schedule(ceil_div_nn(M, BM), ceil_div_nn(N, BN), ceil_div_nn(K, BK),
+                                   capacity, pol);
+  const int v[8] = {s.tiles_m, s.tiles_n, s.kiters, s.grid, s.dp_tiles, s.sk_q, s.sk_r, s.group_m};
+  for (int i = 0; i < 8; ++i) out[i] = v[i];
+  return SGEMM_OK;
+}
+}  // namespace
+
 SGEMM_API int sgemm_schedule_query(int M, int N, int K, int id, int capacity, int* out) {
   if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
   if (id < 0 || id >= kNumConfigs || capacity < 1 || out == nullptr)
     return SGEMM_ERR_INVALID_VALUE;
   const TileShape& S = kConfigs[id]->shape;
-  if ((long long)ceil_div_nn(M, S.BM) * ceil_div_nn(N, S.BN) > 0x7fffffffLL)
-    return SGEMM_ERR_INVALID_DIM;
-  const Schedule s = make_schedule(ceil_div_nn(M, S.BM), ceil_div_nn(N, S.BN),
-                                   ceil_div_nn(K, S.BK), capacity, kGroupM, kMinSplitUnits);
-  const int v[8] = {s.tiles_m, s.tiles_n, s.kiters, s.grid, s.dp_tiles, s.sk_q, s.sk_r, s.group_m};
-  for (int i = 0; i < 8; ++i) out[i] = v[i];
+  SchedPolicy pol;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    pol = g_forced_policy.mode >= 0 ? g_forced_policy : choose_policy(M, N, K);
+  }
+  return schedule_out(M, N, K, S.BM, S.BN, S.BK, capacity, pol, out);
+}
+
+SGEMM_API int sgemm_schedule_plan(int M, int N, int K, int BM, int BN, int BK, int capacity,
+                                  const int* policy, int* out) {
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
+  if (BM < 1 || BN < 1 || BK < 1 || capacity < 1 || policy == nullptr || out == nullptr)
+    return SGEMM_ERR_INVALID_VALUE;
+  const SchedPolicy pol{policy[0], policy[1], policy[2], policy[3]};
+  if (!policy_valid(pol)) return SGEMM_ERR_INVALID_VALUE;
+  return schedule_out(M, N, K, BM, BN, BK, capacity, pol, out);
+}
+
+SGEMM_API int sgemm_force_schedule(const int* policy) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (policy == nullptr || policy[0] < 0) {
+    g_forced_policy.mode = -1;
+    return SGEMM_OK;
+  }
+  const SchedPolicy pol{policy[0], policy[1], policy[2], policy[3]};
+  if (!policy_valid(pol)) return SGEMM_ERR_INVALID_VALUE;
+  g_forced_policy = pol;
+  return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_choose_policy(int M, int N, int K, int* policy) {
+  if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_DIM;
+  if (policy == nullptr) return SGEMM_ERR_INVALID_VALUE;
+  const SchedPolicy p = choose_policy(M, N, K);
+  policy[0] = p.mode;
+  policy[1] = p.group_m;
+  policy[2] = p.min_units;
+  policy[3] = p.splits;
   return SGEMM_OK;
 }
 

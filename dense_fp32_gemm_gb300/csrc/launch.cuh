@@ -73,9 +73,10 @@ struct Launcher {
 
 }  // namespace sgemm_gb300
 
-#define SGEMM_GB300_DEFINE_ENTRY(CFG, VAR) \
-  const ::sgemm_gb300::ConfigEntry VAR =   \
-      ::sgemm_gb300::Launcher<::sgemm_gb300::CFG, false>::entry();
-#define SGEMM_GB300_DEFINE_ENTRY_ALL_LAYOUTS(CFG, VAR) \
-  const ::sgemm_gb300::ConfigEntry VAR =               \
-      ::sgemm_gb300::Launcher<::sgemm_gb300::CFG, true>::entry();
+// The registry entry of configuration NAME (one generated translation unit
+// each): every operand-layout variant when the list marks it ALL_LAYOUTS,
+// else the row-major ones.
+#define SGEMM_GB300_DEFINE_CONFIG(NAME)                                          \
+  namespace sgemm_gb300 {                                                        \
+  const ConfigEntry kEntry##NAME = Launcher<Cfg##NAME, Cfg##NAME::all_layouts>::entry(); \
+  }

@@ -90,10 +90,8 @@ struct NoAllocDevice {
 std::mutex g_na_mutex;
 NoAllocDevice g_na_devices[kNoAllocMaxDevices];  // fixed storage: no heap use
 
-// Same schedule constants as sgemm() and the same automatic tile choice
+// The automatic tile configuration and schedule policy are those of sgemm()
 // (dispatch.hpp), so both entry points run the same kernel and schedule.
-constexpr int kNaGroupM = 8;
-constexpr int kNaMinSplitUnits = 4;
 
 // Once per device, with that device current: symbol address, kernel
 // attributes, occupancy. Called with g_na_mutex held.
@@ -237,8 +235,8 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
 
   const int occ = d->occupancy[id];
   if (occ < 1) return SGEMM_ERR_LAUNCH;
-  const Schedule sched = make_schedule(tiles_m, tiles_n, ceil_div_nn(K, S.BK),
-                                       d->sms * occ, kNaGroupM, kNaMinSplitUnits);
+  const Schedule sched = make_schedule(tiles_m, tiles_n, ceil_div_nn(K, S.BK), d->sms * occ,
+                                       choose_policy(M, N, K));
   const bool split = sched.dp_tiles < sched.tiles;
   const size_t partial_bytes = split ? (size_t)sched.grid * S.BM * S.BN * 4 : 0;
   if ((size_t)sched.grid > kNoAllocMaxFlags ||

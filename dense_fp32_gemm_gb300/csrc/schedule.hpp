@@ -144,38 +144,95 @@ SG_HD bool is_partial_piece(const Schedule& s, const Piece& p) {
   return p.tile >= s.dp_tiles && p.kb != 0;
 }
 
+// How the tile space is decomposed (a per-shape-class choice of the tuner;
+// every mode is exact and deterministic, they differ only in speed):
+//   kSchedHybrid      whole tiles, then the last one to two waves' worth of
+//                     tiles split into k-slice units (with fewer tiles than
+//                     slots, everything is split);
+//   kSchedHybridTail  whole waves of whole tiles; only the ragged last wave
+//                     is split;
+//   kSchedDataParallel whole tiles only, dealt round-robin;
+//   kSchedStreamK     every tile split, the units spread evenly over the slots;
+//   kSchedSplitK      every tile cut into `splits` equal k-ranges, one CTA each
+//                     (capped at the slot count, beyond which it is stream-K).
+// group_m is the raster group height; min_units the fewest k-slices worth
+// giving one CTA when the hybrid and stream-K modes split.
+enum SchedMode : int {
+  kSchedHybrid = 0,
+  kSchedHybridTail = 1,
+  kSchedDataParallel = 2,
+  kSchedStreamK = 3,
+  kSchedSplitK = 4,
+  kNumSchedModes = 5
+};
+
+struct SchedPolicy {
+  int mode;       // SchedMode
+  int group_m;    // raster group height in tiles (>= 1)
+  int min_units;  // >= 1
+  int splits;     // kSchedSplitK: k-ranges per tile (>= 1)
+};
+
+SG_HD bool policy_valid(const SchedPolicy& p) {
+  return p.mode >= 0 && p.mode < kNumSchedModes && p.group_m >= 1 && p.min_units >= 1 &&
+         p.splits >= 1;
+}
+
 // Host-side choice of the decomposition for a problem of batch x tiles_m x
 // tiles_n tiles with kiters k-slices each on `capacity` resident CTA slots.
-// min_units: the fewest k-slices worth giving one CTA in a split.
-inline Schedule make_schedule(int tiles_m, int tiles_n, int kiters, int capacity, int group_m,
-                              int min_units, int batch = 1) {
+inline Schedule make_schedule(int tiles_m, int tiles_n, int kiters, int capacity,
+                              const SchedPolicy& pol, int batch = 1) {
   Schedule s{};
   s.tiles_m = tiles_m;
   s.tiles_n = tiles_n;
   s.tiles = tiles_m * tiles_n * batch;
   s.kiters = kiters;
-  s.group_m = group_m < 1 ? 1 : (group_m > tiles_m ? tiles_m : group_m);
+  s.group_m = pol.group_m < 1 ? 1 : (pol.group_m > tiles_m ? tiles_m : pol.group_m);
   if (s.group_m < 1) s.group_m = 1;
   const int T = s.tiles;
   const int P = capacity < 1 ? 1 : capacity;
+  const int mu = pol.min_units < 1 ? 1 : pol.min_units;
   if (T == 0 || kiters == 0) {
     s.grid = 0;
     return s;
   }
-  if (T % P == 0 || kiters < 2 * min_units) {
-    // whole tiles only: nothing gained by splitting
+  const int64_t units = (int64_t)T * kiters;
+  auto whole = [&]() {
     s.grid = T < P ? T : P;
     s.dp_tiles = T;
-  } else if (T >= P) {
-    // keep all but the last one-to-two waves whole; split those
-    s.grid = P;
-    s.dp_tiles = (T / P - 1) * P;
-  } else {
-    // fewer tiles than slots: split everything, at least min_units per CTA
-    const int64_t units = (int64_t)T * kiters;
-    int64_t g = units / min_units;
-    s.grid = (int)(g < P ? (g < T ? T : g) : P);
+  };
+  // every tile split, over g CTAs (clamped to [1, P]; never more than units)
+  auto split_all = [&](int64_t g) {
+    g = g < 1 ? 1 : (g > P ? P : g);
+    s.grid = (int)(g < units ? g : units);
     s.dp_tiles = 0;
+  };
+  switch (pol.mode) {
+    case kSchedDataParallel:
+      whole();
+      break;
+    case kSchedStreamK:
+      split_all(units / mu);
+      break;
+    case kSchedSplitK: {
+      const int sp = pol.splits < kiters ? pol.splits : kiters;
+      split_all((int64_t)T * (sp < 1 ? 1 : sp));
+      break;
+    }
+    case kSchedHybridTail:
+    default:
+      if (T % P == 0 || kiters < 2 * mu) {
+        whole();  // nothing gained by splitting
+      } else if (T >= P) {
+        // keep whole waves (all but the last one-to-two, in the plain hybrid)
+        s.grid = P;
+        s.dp_tiles = (pol.mode == kSchedHybridTail ? T / P : T / P - 1) * P;
+      } else {
+        // fewer tiles than slots: split everything, at least mu units per CTA
+        const int64_t g = units / mu;
+        split_all(g < T ? T : g);
+      }
+      break;
   }
   s.sk_units = (int64_t)(T - s.dp_tiles) * kiters;
   s.sk_q = (int)(s.sk_units / s.grid);

@@ -680,7 +680,8 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   if (pl.form != kSingle) {
     // groups of 8 tile-row pairs in the raster (measured at 8192^3: 309 against
     // 305 TFLOP/s with 4, 298 with 2; 16 the same as 8)
-    pl.sched = make_schedule((tiles_m + 1) / 2, tiles_n, pl.kiters, pairs, 8, 64 / pl.bk);
+    pl.sched = make_schedule((tiles_m + 1) / 2, tiles_n, pl.kiters, pairs,
+                             SchedPolicy{kSchedHybrid, 8, 64 / pl.bk, 1});
     // every tile split along K: the pairs' lockstep costs more than they save
     // (measured at 1024^3, 1024 x 1024 x 16384 and 16384 x 64 x 4096; the
     // two-SM form gained 4 % at 2048^3 only)
@@ -690,7 +691,8 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
     pl.bk = slice_width(pl.form);
     pl.kiters = ceil_div_nn(K, pl.bk);
     // at least 64 of K per CTA in a split
-    pl.sched = make_schedule(tiles_m, tiles_n, pl.kiters, sms, 8, 64 / pl.bk);
+    pl.sched = make_schedule(tiles_m, tiles_n, pl.kiters, sms,
+                             SchedPolicy{kSchedHybrid, 8, 64 / pl.bk, 1});
   }
   return pl;
 }

@@ -268,8 +268,9 @@ int sgemm_config_layouts(int id);
  * The configuration sgemm() picks by itself for an M x N x K problem (the
  * tuned table's entry for the problem's shape class, ignoring
  * sgemm_force_config). *shape_class (if not NULL) receives the class:
- * 0 square-large, 1 square-small, 2 K-dominant, 3 N <= 96, 4 M <= 96,
- * 5 tiny (at most 2^28 multiply-adds).
+ * 0 square-large (M * N >= 12 Mi), 1 square-small (M * N < 3 Mi),
+ * 2 K-dominant (K >= 4 max(M, N)), 3 N <= 96, 4 M <= 96, 5 tiny (at most
+ * 2^28 multiply-adds), 6 square-mid (3 Mi <= M * N < 12 Mi).
  * Returns the configuration id or SGEMM_ERR_INVALID_DIM. Host only.
  * Pages: "Autotuning: Searching the Tile-Shape Space" picks one configuration
  * by measurement for one shape ("What The Sweep Found") and notes that the
@@ -294,12 +295,59 @@ int sgemm_cfg_check(const int* params, int* derived);
 /*
  * The persistent schedule sgemm() would use for an M x N x K problem with
  * configuration `id` on `capacity` resident CTAs (host arithmetic only, no
- * device needed). out = {tiles_m, tiles_n, kiters, grid, dp_tiles, sk_q,
- * sk_r, group_m}. Returns SGEMM_OK or an argument error.
+ * device needed), under the policy sgemm() would take (a forced one, else
+ * the tuned policy of the problem's shape class). out = {tiles_m, tiles_n,
+ * kiters, grid, dp_tiles, sk_q, sk_r, group_m}. Returns SGEMM_OK or an
+ * argument error.
  * The pages launch one CTA per C tile ("Shared Memory Tiling", kernel launch
  * grid); the persistent schedule is this library's (silent on the pages).
  */
 int sgemm_schedule_query(int M, int N, int K, int id, int capacity, int* out);
+
+/*
+ * Persistent-schedule policies (the values of policy[0]):
+ *   SGEMM_SCHED_HYBRID      whole tiles, then the last one to two waves' worth
+ *                           of tiles split into k-slice units (with fewer
+ *                           tiles than CTA slots, every tile is split);
+ *   SGEMM_SCHED_HYBRID_TAIL whole waves of whole tiles; only the ragged last
+ *                           wave is split;
+ *   SGEMM_SCHED_DATA_PARALLEL whole tiles only;
+ *   SGEMM_SCHED_STREAM_K    every tile split, the k-slice units spread evenly;
+ *   SGEMM_SCHED_SPLIT_K     every tile cut into policy[3] equal k-ranges.
+ * A policy is int[4] = {mode, raster group height in tiles (>= 1), fewest
+ * k-slices per CTA when splitting (>= 1), splits (>= 1)}. Every policy gives
+ * a correct result; split partial sums are added in a fixed order, so a
+ * policy always gives the same bits. The pages are silent (one CTA per tile).
+ */
+#define SGEMM_SCHED_HYBRID 0
+#define SGEMM_SCHED_HYBRID_TAIL 1
+#define SGEMM_SCHED_DATA_PARALLEL 2
+#define SGEMM_SCHED_STREAM_K 3
+#define SGEMM_SCHED_SPLIT_K 4
+
+/*
+ * The schedule of an M x N x K problem with BM x BN tiles and BK-wide
+ * k-slices on `capacity` CTA slots under `policy` (host arithmetic only):
+ * out as for sgemm_schedule_query. Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM
+ * (negative size, or more than 2^31 - 1 tiles) or SGEMM_ERR_INVALID_VALUE.
+ */
+int sgemm_schedule_plan(int M, int N, int K, int BM, int BN, int BK, int capacity,
+                        const int* policy, int* out);
+
+/*
+ * Forces `policy` on every later sgemm(), sgemm_ex() and
+ * sgemm_strided_batched() call of this process (the tuner and tests); NULL or
+ * policy[0] < 0 restores the tuned policy of each problem's shape class.
+ * Returns SGEMM_OK or SGEMM_ERR_INVALID_VALUE (nothing changed).
+ */
+int sgemm_force_schedule(const int* policy);
+
+/*
+ * The tuned policy sgemm() uses by itself for an M x N x K problem (that of
+ * its shape class), written to policy[4]. Returns SGEMM_OK or an argument
+ * error. Host only.
+ */
+int sgemm_choose_policy(int M, int N, int K, int* policy);
 
 /*
  * Piece `i` of CTA `b` under the schedule {tiles_m, tiles_n, kiters, grid,

@@ -17,9 +17,8 @@ def compiled_config_count():
     """Number of tile configurations in the library, read from the config
     list in the sources (so collecting tests never needs the library)."""
     import re
-    text = open(os.path.join(ROOT, "dense_fp32_gemm_gb300", "csrc", "configs.hpp")).read()
+    text = open(os.path.join(ROOT, "dense_fp32_gemm_gb300", "csrc", "configs.inc")).read()
     block = text[text.index("#define SGEMM_GB300_CONFIGS(X)"):]
-    block = block[: block.index("\n\n")]
     return len(re.findall(r"^\s*X\(", block, flags=re.M))
 
 
