@@ -2,12 +2,15 @@
 // with the host <-> device copies overlapped with the GEMM.
 //
 // K is cut into chunks. While the GPU multiplies chunk i (A[:, Ki] * B[Ki, :],
-// accumulated into a device copy of C), the copy engine brings in chunk i+1;
-// the first chunk is narrow so the first multiply starts early. The incoming C
-// needed for beta * C travels on the same copy stream after the operand
-// chunks. The last chunk is multiplied in row panels: as soon as a panel is
-// final (beta * C added) it is copied back on a second copy stream while the
-// next panel computes. The caller's stream waits for the last copy, so
+// accumulated into a device copy of C), the copy engine brings in chunk i+1.
+// The chunks grow geometrically: the first is narrow so the first multiply
+// starts early, and each next one is as many times wider as multiplying a
+// column of K takes longer than copying it, so every copy hides under the
+// previous multiply. The incoming C needed for beta * C travels on the same
+// copy stream after the operand chunks, one row panel at a time. The last
+// chunk is multiplied in row panels: as soon as a panel is final (beta * C
+// added) it is copied back on a second copy stream while the next panel
+// computes. The caller's stream waits for the last copy, so
 // synchronising the caller's stream means C (host) is final. Splitting K only
 // reorders the sum over k; results stay within the FP32 tolerance and integer
 // inputs stay exact.
@@ -36,16 +39,49 @@ constexpr int kMaxPanels = 8;
 // The copy/compute pipeline: K chunk widths and the row panels of the last
 // chunk (sgemm_host_set_pipeline). Widths are rounded up to multiples of 32.
 struct Pipeline {
-  int first = 256;   // first chunk (only when K >= 2 * first + last)
-  int mid = 1024;    // target width of the chunks between the first and the last
-  int last = 0;      // last chunk; 0: as wide as the middle chunks
+  int first = 128;   // first chunk
+  int mid = 0;       // 0: geometric growth; > 0: equal chunks of about `mid`
+                     // between the first and the last
+  int last = 0;      // last chunk; 0: what the growth leaves (geometric), or as
+                     // wide as the middle chunks (equal)
   int panels = 4;    // row panels of the last chunk (only when M >= 512 * panels)
 };
 Pipeline g_pipe;
 
-// Chunk boundaries 0 = kb[0] < ... < kb[n] = K for a K-wide problem.
-int chunk_bounds(int K, const Pipeline& pp, int* kb) {
-  auto r32 = [](int x) { return (x + 31) / 32 * 32; };
+// Growth of the geometric chunk widths for an M x N result: multiplying one
+// column of K costs 2 M N flops (about 68 TFLOP/s), copying it 4 (M + N)
+// bytes (about 200 GB/s from pinned memory), so a chunk may be
+// M N / (M + N) / 680 times wider than the previous one and still copy within
+// the previous multiply; with a 10 % margin, clamped to [1.5, 4].
+double chunk_growth(int M, int N) {
+  const double g = (double)M * N / ((double)M + N) / 755.0;
+  return g < 1.5 ? 1.5 : (g > 4.0 ? 4.0 : g);
+}
+
+// Chunk boundaries 0 = kb[0] < ... < kb[n] = K for an M x N x K problem;
+// returns the chunk count n (at most kMaxChunks).
+int chunk_bounds(int M, int N, int K, const Pipeline& pp, int* kb) {
+  auto r32 = [](long long x) { return (int)((x + 31) / 32 * 32); };
+  if (pp.mid == 0) {
+    const int last = pp.last > 0 ? r32(pp.last) : 0;
+    const int k_hi = (last > 0 && K > last) ? K - last : K;
+    const int budget = kMaxChunks - (k_hi < K ? 1 : 0);
+    const double g = chunk_growth(M, N);
+    int n = 0, k = 0, w = r32(pp.first > 0 ? pp.first : 128);
+    kb[0] = 0;
+    while (k < k_hi) {
+      int wc = w < k_hi - k ? w : k_hi - k;
+      const int next = r32((long long)(wc * g));
+      // a remainder narrower than half the next chunk joins this one, and so
+      // does everything once the chunk budget is used up
+      if (k_hi - (k + wc) < next / 2 || n + 1 >= budget) wc = k_hi - k;
+      k += wc;
+      kb[++n] = k;
+      w = next;
+    }
+    if (k_hi < K) kb[++n] = K;
+    return n;
+  }
   const int first = r32(pp.first), last = pp.last > 0 ? r32(pp.last) : 0;
   int n = 0;
   kb[n++] = 0;
@@ -69,7 +105,7 @@ struct HostCtx {
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t start = nullptr, chunk[kMaxChunks] = {}, panel[kMaxPanels] = {}, c_in = nullptr,
-              done = nullptr, out = nullptr;
+              done = nullptr, out = nullptr, c_in_panel[kMaxPanels] = {};
   float *dA = nullptr, *dB = nullptr, *dC = nullptr, *dC0 = nullptr;
   size_t capA = 0, capB = 0, capC = 0, capC0 = 0;  // floats
 };
@@ -111,7 +147,8 @@ int ctx_for(int dev, cudaStream_t user, HostCtx** out) {
         return SGEMM_ERR_LAUNCH;
       }
     for (int i = 0; i < kMaxPanels; ++i)
-      if (cudaEventCreateWithFlags(&c.panel[i], cudaEventDisableTiming) != cudaSuccess) {
+      if (cudaEventCreateWithFlags(&c.panel[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&c.c_in_panel[i], cudaEventDisableTiming) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
       }
@@ -158,7 +195,10 @@ void host_api_release() {
       cudaEventDestroy(c.done);
       cudaEventDestroy(c.out);
       for (int i = 0; i < kMaxChunks; ++i) cudaEventDestroy(c.chunk[i]);
-      for (int i = 0; i < kMaxPanels; ++i) cudaEventDestroy(c.panel[i]);
+      for (int i = 0; i < kMaxPanels; ++i) {
+        cudaEventDestroy(c.panel[i]);
+        cudaEventDestroy(c.c_in_panel[i]);
+      }
     }
   }
   g_host.clear();
@@ -229,7 +269,7 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
     // K chunk boundaries: a narrow first chunk, equal middle chunks, and a
     // last chunk that is computed (and copied back) in row panels
     int kb[kMaxChunks + 2];
-    const int nk = chunk_bounds(K, g_pipe, kb);
+    const int nk = chunk_bounds(M, N, K, g_pipe, kb);
     for (int i = 0; i < nk; ++i) {
       const int k0 = kb[i], k1 = kb[i + 1];
       if (cudaMemcpy2DAsync(c->dA + k0, (size_t)K * 4, A + k0, (size_t)lda * 4,
@@ -239,11 +279,19 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
           cudaEventRecord(c->chunk[i], c->h2d) != cudaSuccess)
         return fail();
     }
+    // row panels of the last chunk
+    const int panels = M >= 512 * g_pipe.panels ? g_pipe.panels : (M >= 1024 ? M / 512 : 1);
+    const int rows = ((M + panels - 1) / panels + 127) / 128 * 128;
+    // the incoming C, one row panel at a time: panel p's add waits only for
+    // its own rows
     if (beta != 0.f) {
-      if (cudaMemcpy2DAsync(c->dC0, row_c, C, pitch_c, row_c, M, cudaMemcpyHostToDevice,
-                            c->h2d) != cudaSuccess ||
-          cudaEventRecord(c->c_in, c->h2d) != cudaSuccess)
-        return fail();
+      for (int pi = 0, r0 = 0; r0 < M; ++pi, r0 += rows) {
+        const int r1 = (r0 + rows < M) ? r0 + rows : M;
+        if (cudaMemcpy2DAsync(c->dC0 + (size_t)r0 * N, row_c, C + (size_t)r0 * ldc, pitch_c, row_c,
+                              r1 - r0, cudaMemcpyHostToDevice, c->h2d) != cudaSuccess ||
+            cudaEventRecord(c->c_in_panel[pi], c->h2d) != cudaSuccess)
+          return fail();
+      }
     }
     for (int i = 0; i + 1 < nk; ++i) {
       if (cudaStreamWaitEvent(user, c->chunk[i], 0) != cudaSuccess) return fail();
@@ -253,10 +301,7 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
     }
     // last chunk in row panels, each copied back as soon as it is final
     const int k0 = kb[nk - 1], kl = K - k0;
-    const int panels = M >= 512 * g_pipe.panels ? g_pipe.panels : (M >= 1024 ? M / 512 : 1);
-    const int rows = ((M + panels - 1) / panels + 127) / 128 * 128;
     if (cudaStreamWaitEvent(user, c->chunk[nk - 1], 0) != cudaSuccess) return fail();
-    if (beta != 0.f && cudaStreamWaitEvent(user, c->c_in, 0) != cudaSuccess) return fail();
     for (int pi = 0, r0 = 0; r0 < M; ++pi, r0 += rows) {
       const int r1 = (r0 + rows < M) ? r0 + rows : M;
       float* dCp = c->dC + (size_t)r0 * N;
@@ -265,6 +310,7 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
       if (st != SGEMM_OK) return st;
       const size_t pn = (size_t)(r1 - r0) * N;
       if (beta != 0.f) {
+        if (cudaStreamWaitEvent(user, c->c_in_panel[pi], 0) != cudaSuccess) return fail();
         int pb = (int)((pn + 255) / 256);
         if (pb > sms * 8) pb = sms * 8;
         add_scaled_kernel<<<pb, 256, 0, user>>>((long long)pn, beta, dCp, c->dC0 + (size_t)r0 * N);
@@ -297,8 +343,9 @@ SGEMM_API int sgemm_host_set_pipeline(int first, int mid, int last, int panels) 
   std::lock_guard<std::mutex> lock(g_host_mutex);
   const Pipeline defaults;
   g_pipe.first = first;
-  g_pipe.mid = mid > 0 ? mid : defaults.mid;
+  g_pipe.mid = mid;
   g_pipe.last = last;
   g_pipe.panels = panels > 0 ? panels : defaults.panels;
+  if (mid == 0 && first == 0) g_pipe.first = defaults.first;
   return SGEMM_OK;
 }

@@ -175,9 +175,11 @@ int sgemm_strided_batched(int opA, int opB, int M, int N, int K, float alpha, co
  * The same C = alpha * A * B + beta * C with A, B and C in HOST memory (pinned
  * memory gives full copy bandwidth; pageable memory works but the copies may
  * block the calling thread). K is cut into chunks whose host -> device copies
- * overlap the multiplication of the previous chunk on the GPU; the incoming C
- * (read only when beta != 0) is added by one elementwise pass at the end;
- * the result is copied back. All work is queued behind earlier work on
+ * overlap the multiplication of the previous chunk on the GPU (by default the
+ * chunks grow geometrically, each as much wider as multiplying a column of K
+ * takes longer than copying it); the incoming C (read only when beta != 0)
+ * arrives in row panels and is added panel by panel at the end, and each
+ * finished row panel is copied back while the next one is computed. All work is queued behind earlier work on
  * `stream`, and `stream` waits for the final copy: once the caller has
  * synchronised `stream`, C holds the result. The host buffers must stay
  * valid until then. Device buffers, two copy streams and their events are
@@ -189,12 +191,17 @@ int sgemm_host(int M, int N, int K, float alpha, const float* A, int lda, const 
                float beta, float* C, int ldc, void* stream);
 
 /*
- * Copy/compute pipeline of later sgemm_host calls (process-wide): K is cut
- * into a first chunk of `first` columns (0: none; taken only when K >= 2 *
- * first + last), middle chunks of about `mid` columns (0: 1024), and a last
- * chunk of `last` columns (0: as wide as the middle chunks) that is computed
- * and copied back in `panels` row panels (0: 4; at most 8; fewer when M <
- * 512 * panels). Widths are rounded up to multiples of 32; at most 9 chunks.
+ * Copy/compute pipeline of later sgemm_host calls (process-wide). With
+ * mid == 0 (the default) K is cut into geometrically growing chunks: a first
+ * chunk of `first` columns (0: 128), each next one min(4, max(1.5,
+ * M N / (M + N) / 755)) times wider, a remainder narrower than half the next
+ * width joining the chunk before it, and, when last > 0, a last chunk of
+ * `last` columns. With mid > 0: a first chunk of `first` columns (0: none;
+ * taken only when K >= 2 * first + last), middle chunks of about `mid`
+ * columns, and a last chunk of `last` columns (0: as wide as the middle
+ * chunks). The last chunk is computed and copied back in `panels` row panels
+ * (0: 4; at most 8; fewer when M < 512 * panels). Widths are rounded up to
+ * multiples of 32; at most 9 chunks.
  * The result does not depend on the setting beyond the order of the sum
  * over k. Returns SGEMM_ERR_INVALID_VALUE (nothing changed) for a negative
  * value or more than 8 panels. The pages are silent.

@@ -71,9 +71,11 @@ def test_host_full_size_integer():
 
 
 @pytest.mark.parametrize("pipeline", [(128, 512, 256, 8), (0, 4096, 0, 1), (256, 1024, 512, 2),
-                                      (64, 64, 64, 3)], ids=lambda p: "-".join(map(str, p)))
+                                      (64, 64, 64, 3), (32, 0, 0, 8), (64, 0, 512, 3), (2048, 0, 0, 2)],
+                         ids=lambda p: "-".join(map(str, p)))
 def test_host_pipeline_settings(pipeline):
-    # any chunking of K and any panel count give the same (exact) result
+    # any chunking of K (equal middle chunks, or geometric growth when mid is
+    # 0) and any panel count give the same (exact) result
     assert binding.sgemm_host_set_pipeline(*pipeline) == 0
     try:
         _host_call(Workload("hostpipe", 2100, 300, 3000, 1.25, -0.5, "int3", 88))

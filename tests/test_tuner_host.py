@@ -142,3 +142,13 @@ def test_every_class_dispatches_to_an_all_layout_configuration():
             cid, _ = binding.sgemm_choose_config(M, N, K)
             assert binding.sgemm_config_layouts(cid) == 1, (cls, binding.sgemm_config_info(cid)[0])
     assert binding.sgemm_config_layouts(binding.sgemm_config_count()) == binding.SGEMM_ERR_INVALID_VALUE
+
+
+def test_default_policy_wins_within_noise():
+    D, S = tune.DEFAULT_POLICY, (tune.SPK, 8, 4, 2)
+    t = {("a", D): [1.003, 2.0], ("a", S): [1.0, 2.0], ("b", D): [1.5, 3.0]}
+    assert tune.pick_with_default(t) == ("a", D)            # 0.15 % behind: noise
+    t[("a", S)] = [0.9, 1.8]
+    assert tune.pick_with_default(t) == ("a", S)            # 10 % ahead: a real win
+    rec = {"stage2_ms": {"tiny": {f"a {list(D)}": [1.003], f"a {list(S)}": [1.0]}}}
+    assert tune.winners_from_record(rec) == {"tiny": ("a", D)}
