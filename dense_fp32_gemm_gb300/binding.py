@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
                 "sgemm_config_count": (I, []),
                 "sgemm_config_info": (I, [I, ctypes.c_char_p, I, IP]),
                 "sgemm_force_config": (I, [I]),
+                "sgemm_set_staged_a": (I, [I]),
                 "sgemm_cfg_check": (I, [IP, IP]),
                 "sgemm_schedule_query": (I, [I, I, I, I, I, IP]),
                 "sgemm_schedule_piece": (I, [IP, I, I, IP]),
@@ -168,6 +169,13 @@ def sgemm_shutdown() -> None:
 
 def sgemm_config_count() -> int:
     return lib().sgemm_config_count()
+
+
+def sgemm_set_staged_a(on: int) -> int:
+    """Row-major A through the staging ring and producer warp: 1 where allowed
+    and each CTA runs at least 8 k-slices (default), 2 wherever allowed, 0
+    never (the transposing copy). Returns the previous setting."""
+    return lib().sgemm_set_staged_a(on)
 
 
 def sgemm_config_info(cid: int):

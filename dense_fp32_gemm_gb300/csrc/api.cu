@@ -42,6 +42,13 @@ static_assert(kNumConfigIds == kNumConfigs, "config ids");
 
 std::mutex g_mutex;
 std::atomic<int> g_forced{-1};
+// Row-major A through the staging ring and producer warp (ALoad kARowStg)
+// where the configuration is built with it and A is TMA-aligned
+// (sgemm_set_staged_a): 1 where each CTA also runs at least kStagedMinSteps
+// k-slices, 2 whatever the size, 0 never (the transposing copy everywhere).
+std::atomic<int> g_staged_a{1};
+// Fewest k-slices per CTA (on average) for which the staged variant is used.
+constexpr int kStagedMinSteps = 8;
 // A schedule policy forced for every later call (tuner, tests); mode < 0:
 // the tuned policy of the problem's shape class. Guarded by g_mutex.
 SchedPolicy g_forced_policy{-1, 8, 4, 1};
@@ -53,6 +60,7 @@ struct DeviceInfo {
   bool supported = false;
   int sms = 0;
   int occupancy[kNumConfigs] = {};  // resident CTAs per SM
+  int occupancy_staged[kNumConfigs] = {};  // same, staged-A variant (0: not built)
 };
 std::map<int, DeviceInfo> g_devices;
 
@@ -85,6 +93,10 @@ int device_info(int dev, DeviceInfo** out) {
         int blocks = 0;
         if (kConfigs[c]->occupancy(&blocks) != cudaSuccess) return SGEMM_ERR_LAUNCH;
         d.occupancy[c] = blocks;
+        blocks = 0;
+        if (kConfigs[c]->staged && kConfigs[c]->occupancy_staged(&blocks) != cudaSuccess)
+          return SGEMM_ERR_LAUNCH;
+        d.occupancy_staged[c] = blocks;
       }
     }
     d.ready = true;
@@ -180,15 +192,15 @@ __global__ void scale_c_kernel(int M, int N, float beta, float* C, long long ldc
 // matrix pitch stride, in elements) with a box of box_cols x box_rows x 1.
 bool encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const float* base,
                int cols, int rows, long long ld, long long stride, int batch, int box_cols,
-               int box_rows) {
+               int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   const long long pitch2 = batch > 1 ? stride : ld * (rows > 0 ? rows : 1);
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
   cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)(((pitch2 * 4) + 15) / 16 * 16)};
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Argument checks shared by every FFMA entry point; 0 when valid.
@@ -289,6 +301,20 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
   const long long total_tiles = (long long)tiles_m * tiles_n * batch;
   if (total_tiles > 0x7fffffffLL) return SGEMM_ERR_INVALID_DIM;
   Schedule sched = make_schedule(tiles_m, tiles_n, kiters, di->sms * occ, policy, batch);
+  // row-major A with B by TMA: the staged variant where it is built, keeps
+  // the configuration's residency, A is TMA-aligned (a K x M box of 32 x BM,
+  // 128-byte swizzled), and each CTA runs enough k-slices to cover the extra
+  // step of latency the staging adds before the first FMA (measured on
+  // GB300: 4 k-slices per CTA at 512^3 lose 5 %, 13 at 1024^3 gain 4 %)
+  const int staged_mode = g_staged_a.load();
+  if (al == kARow && bl == kBRowTma && cfg.staged && staged_mode != 0 &&
+      di->occupancy_staged[id] == occ &&
+      (staged_mode == 2 ||
+       (long long)sched.tiles * kiters >= (long long)kStagedMinSteps * sched.grid) &&
+      ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0) &&
+      (single || (sA & 3) == 0) &&
+      encode_3d(enc, &map_a, A, K, M, lda, sA, batch, S.BK, S.BM, CU_TENSOR_MAP_SWIZZLE_128B))
+    al = kARowStg;
 
   const bool split = sched.dp_tiles < sched.tiles;
   Workspace* ws = nullptr;
@@ -325,7 +351,7 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
     cudaGetLastError();
     return SGEMM_ERR_LAUNCH;
   }
-  static const char* const kAName[] = {"a=rowT", "a=tma", "a=cp"};
+  static const char* const kAName[] = {"a=rowT", "a=tma", "a=cp", "a=stg"};
   static const char* const kBName[] = {"b=tma", "b=cp", "b=colT"};
   snprintf(g_last_config, sizeof(g_last_config),
            "%s %s %s grid=%d dp=%d split=%d kiters=%d sched=%d/g%d/u%d/s%d%s", cfg.name,
@@ -519,6 +545,11 @@ SGEMM_API int sgemm_config_info(int id, char* name, int len, int* params) {
 SGEMM_API int sgemm_config_layouts(int id) {
   if (id < 0 || id >= kNumConfigs) return SGEMM_ERR_INVALID_VALUE;
   return kConfigs[id]->all_layouts ? 1 : 0;
+}
+
+SGEMM_API int sgemm_set_staged_a(int on) {
+  if (on < 0 || on > 2) return SGEMM_ERR_INVALID_VALUE;
+  return g_staged_a.exchange(on);
 }
 
 SGEMM_API int sgemm_force_config(int id) {

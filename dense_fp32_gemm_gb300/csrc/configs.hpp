@@ -56,6 +56,8 @@ struct ConfigEntry {
   AttrFn set_attributes;
   OccFn occupancy;
   LaunchFn launch;
+  bool staged;         // built with the staged-A variant (ALoad kARowStg)
+  OccFn occupancy_staged;  // its resident CTAs per SM (0 when not built)
 };
 
 // Registry index of each configuration: kId<Name>.

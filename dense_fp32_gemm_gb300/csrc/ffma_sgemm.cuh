@@ -84,19 +84,26 @@ struct KernelParams {
 //   A: kARow   A stored M x K (op N): transposing 4-byte cp.async into As[k][m]
 //      kATTma  A stored K x M (op T): one 3-D TMA box, As[k][m] needs no transpose
 //      kATCp   A stored K x M (op T): plain 4-byte cp.async (A not TMA-aligned)
+//      kARowStg A stored M x K (op N), TMA-aligned: one 3-D TMA box per k-slice
+//              into a staging slot as stored, transposed into As[k][m] by an
+//              extra producer warp (with B by TMA only; tile_config.hpp,
+//              stg_eligible); the FMA warps then issue no copies at all
 //   B: kBRowTma B stored K x N (op N): one 3-D TMA box into Bs[k][n]
 //      kBRowCp  B stored K x N (op N): plain 4-byte cp.async
 //      kBT      B stored N x K (op T): transposing 4-byte cp.async into Bs[k][n]
-enum ALoad : int { kARow = 0, kATTma = 1, kATCp = 2 };
+enum ALoad : int { kARow = 0, kATTma = 1, kATCp = 2, kARowStg = 3 };
 enum BLoad : int { kBRowTma = 0, kBRowCp = 1, kBT = 2 };
 
 // Shared-memory layout (from a 1024-byte aligned base):
 //   Bs[STAGES][BK][BP] | As[STAGES][BK][AP] | fullA[STAGES] | fullB[STAGES] |
 //   empty[STAGES] | sync barrier | abort word
+// and for kARowStg (with the ring depth of stg_ring_stages):
+//   Bs | As | staging[kStgSlots][BM][BK] | the barrier block | staged[kStgSlots]
 // with row pitches AP = BM (+ kApad when transposed on store) and likewise BP.
 template <int ST>
 struct BarrierBlock {
-  uint64_t fullA[ST];   // NT cp.async arrivals: this thread's copies landed
+  uint64_t fullA[ST];   // NT cp.async arrivals: this thread's copies landed (kARowStg:
+                        // one arrival per producer lane once it has stored its part)
   uint64_t fullB[ST];   // one expect_tx arrival + the TMA transaction bytes of the stage
   uint64_t empty[ST];   // one arrival per warp: the slot may be refilled
   uint64_t sync;        // CTA-wide rendezvous with a bounded wait
@@ -108,6 +115,18 @@ constexpr int kernel_smem_bytes() {
   constexpr TileShape S = Cfg::S;
   static_assert(sizeof(BarrierBlock<S.STAGES>) <= S.STAGES * 3 * 8 + 16, "barrier block size");
   return smem_bytes(S);
+}
+template <class Cfg>
+constexpr int kernel_smem_bytes_stg() {
+  constexpr TileShape S = Cfg::S;
+  constexpr int ST = stg_ring_stages(S);
+  static_assert(sizeof(BarrierBlock<ST>) <= ST * 3 * 8 + 16, "barrier block size");
+  return stg_smem_bytes(S, ST);
+}
+// Threads of one CTA: the FMA warps, plus the producer warp of kARowStg.
+template <class Cfg, int AL>
+constexpr int kernel_threads() {
+  return Cfg::S.NT + (AL == kARowStg ? kWarp : 0);
 }
 
 // Bound of the clean-up waits of an aborting CTA (copies and MMAs it already
@@ -158,17 +177,20 @@ __device__ __forceinline__ void issue_a_tile(uint32_t dst, const float* src, lon
 }
 
 template <class Cfg, int AL, int BL>
-__global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
+__global__ void __launch_bounds__(kernel_threads<Cfg, AL>(), Cfg::S.MINB)
     ffma_sgemm_kernel(const __grid_constant__ KernelParams p,
                       const __grid_constant__ CUtensorMap tmapA,
                       const __grid_constant__ CUtensorMap tmapB) {
   constexpr TileShape S = Cfg::S;
   static_assert(cfg_valid(S), "illegal tile configuration");
-  constexpr int BM = S.BM, BN = S.BN, BK = S.BK, NT = S.NT, ST = S.STAGES, KU = S.KU;
+  constexpr bool kStg = (AL == kARowStg);
+  static_assert(!kStg || (stg_eligible(S) && BL == kBRowTma), "staged A needs an eligible shape");
+  constexpr int BM = S.BM, BN = S.BN, BK = S.BK, NT = S.NT, KU = S.KU;
+  constexpr int ST = kStg ? stg_ring_stages(S) : S.STAGES;
   constexpr int ORDER = S.ORDER;
   constexpr int WM = S.WM, WN = S.WN, TM = S.TM, TN = S.TN, WNITER = S.WNITER;
   constexpr int WMITER = wmiter(S), WSUBM = wsubm(S), WSUBN = wsubn(S);
-  constexpr int AP = (AL == kARow) ? BM + kApad : BM;   // As row pitch (floats)
+  constexpr int AP = (AL == kARow || kStg) ? BM + kApad : BM;  // As row pitch (floats)
   constexpr int BP = (BL == kBT) ? BN + kApad : BN;     // Bs row pitch (floats)
   constexpr int A_ST = a_stage_floats(S), B_ST = b_stage_floats(S);
   static_assert(BK * AP <= A_ST && BK * BP <= B_ST, "stage sizes");
@@ -185,8 +207,10 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   constexpr int B_PASSES = (BK * BN) / NT;
   constexpr int AT_PASSES = (BK * BM) / NT;
   constexpr int WARPS_N = BN / WN;
-  constexpr bool kUsesCp = (AL != kATTma) || (BL != kBRowTma);
+  constexpr bool kUsesCp = (AL != kATTma && !kStg) || (BL != kBRowTma);
   constexpr bool kUsesTma = (AL == kATTma) || (BL == kBRowTma);
+  // the FMA warps wait for fullA when A arrives by copies or from the producer
+  constexpr bool kWaitA = kUsesCp || kStg;
   constexpr uint32_t TMA_BYTES =
       (uint32_t)(((AL == kATTma) ? BK * BM * 4 : 0) + ((BL == kBRowTma) ? BK * BN * 4 : 0));
   constexpr uint32_t FULL = 0xffffffffu;
@@ -196,7 +220,10 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   unsigned char* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   float* Bs = reinterpret_cast<float*>(base);
   float* As = Bs + ST * B_ST;
-  BarrierBlock<ST>* bb = reinterpret_cast<BarrierBlock<ST>*>(As + ST * A_ST);
+  float* Stg = As + ST * A_ST;  // kARowStg staging slots (1024-byte aligned)
+  BarrierBlock<ST>* bb =
+      reinterpret_cast<BarrierBlock<ST>*>(Stg + (kStg ? kStgSlots * BM * BK : 0));
+  uint64_t* staged = reinterpret_cast<uint64_t*>(bb + 1);  // kARowStg: slot landed
   volatile int* abort_w = &bb->abort;
 
   const int tid = threadIdx.x;
@@ -207,20 +234,161 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&bb->fullA[s]), NT);
+      ptx::mbar_init(ptx::smem_addr(&bb->fullA[s]), kStg ? kWarp : NT);
       ptx::mbar_init(ptx::smem_addr(&bb->fullB[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&bb->empty[s]), NT / 32);
     }
     ptx::mbar_init(ptx::smem_addr(&bb->sync), NT);
+    if (kStg)
+      for (int j = 0; j < kStgSlots; ++j) ptx::mbar_init(ptx::smem_addr(&staged[j]), 1);
     bb->abort = 0;
     ptx::mbar_fence_init();
-    if (AL == kATTma) ptx::tma_prefetch_desc(&tmapA);
+    if (AL == kATTma || kStg) ptx::tma_prefetch_desc(&tmapA);
     if (BL == kBRowTma) ptx::tma_prefetch_desc(&tmapB);
   }
   __syncthreads();
 
   const int npieces = num_pieces(sc, b);
   const int nsteps = (int)total_steps(sc, b);
+
+  if constexpr (kStg) {
+    if (warp == NT / kWarp) {
+      // ---- the producer warp of kARowStg --------------------------------------
+      // Walks the same steps as the FMA warps. Step s: wait until ring slot
+      // s % ST is free, start the TMA of its B tile, wait for the staged A
+      // slice of step s, transpose it into the slot's As[k][m] and arrive on
+      // fullA; then start the staging TMA of step s + kStgSlots into the
+      // staging slot just read. A slice is thus requested kStgSlots steps
+      // before it is transposed, and the B tile of a step as soon as its slot
+      // is free.
+      struct Cursor {
+        int piece, k, ke, m0, n0, bi;
+      };
+      auto cur_set = [&](Cursor& c, int i) {
+        const Piece lp = get_piece(sc, b, i);
+        int tm, tn;
+        tile_coords_batched(sc, lp.tile, c.bi, tm, tn);
+        c.piece = i;
+        c.k = lp.kb;
+        c.ke = lp.ke;
+        c.m0 = tm * BM;
+        c.n0 = tn * BN;
+      };
+      auto cur_next = [&](Cursor& c) {
+        if (++c.k == c.ke && c.piece + 1 < npieces) cur_set(c, c.piece + 1);
+      };
+      Cursor ca{0, 0, 0, 0, 0, 0}, cb{0, 0, 0, 0, 0, 0};
+      if (npieces > 0) {
+        cur_set(ca, 0);
+        cur_set(cb, 0);
+      }
+      const uint32_t stg_addr = ptx::smem_addr(Stg);
+      constexpr uint32_t kStgBytes = (uint32_t)(BM * BK * 4);
+      int a_issued = 0, b_issued = 0, s = 0;
+      auto issue_staging = [&]() {
+        if (lane == 0) {
+          const int j = a_issued % kStgSlots;
+          const uint32_t fa = ptx::smem_addr(&staged[j]);
+          ptx::mbar_arrive_expect_tx(fa, kStgBytes);
+          ptx::tma_load_3d(stg_addr + (uint32_t)j * kStgBytes, &tmapA, ca.k * BK, ca.m0, ca.bi, fa);
+        }
+        ++a_issued;
+        cur_next(ca);
+      };
+      // One staging slot (BM rows of 32 k-values, 128-byte rows; TMA's 128-byte
+      // swizzle keeps 16-byte chunk c of row r at chunk c ^ (r & 7)) into
+      // As[k][m]: the lane moves 4 x 4 blocks e = q * 32 + lane, rows 4 rg ..
+      // 4 rg + 3 with rg = e % (BM / 4), k-chunk c = (e / (BM / 4) + rg) % 8,
+      // with four 128-bit loads and four 128-bit stores. Each group of eight
+      // lanes then reads eight different chunk positions and writes eight
+      // different 16-byte bank groups (the row pitch BM + 4 shifts each k-row
+      // by one group), so neither side has bank conflicts.
+      auto transpose_slot = [&](const float* src, float* dst) {
+        constexpr int R = BM / 4, NB = BM / 16, UB = NB < 4 ? NB : 4;
+        static_assert(NB % UB == 0, "staging blocks per lane");
+        const char* sb = reinterpret_cast<const char*>(src);
+#pragma unroll
+        for (int q0 = 0; q0 < NB; q0 += UB) {
+          float4 v[UB][4];
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const int e = (q0 + u) * kWarp + lane;
+            const int rg = e % R, c = (e / R + rg) & 7;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = 4 * rg + j;
+              v[u][j] = *reinterpret_cast<const float4*>(sb + r * 128 + ((c ^ (r & 7)) << 4));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const int e = (q0 + u) * kWarp + lane;
+            const int rg = e % R, c = (e / R + rg) & 7;
+            float* d = dst + (4 * c) * AP + 4 * rg;
+            *reinterpret_cast<float4*>(d + 0 * AP) =
+                make_float4(v[u][0].x, v[u][1].x, v[u][2].x, v[u][3].x);
+            *reinterpret_cast<float4*>(d + 1 * AP) =
+                make_float4(v[u][0].y, v[u][1].y, v[u][2].y, v[u][3].y);
+            *reinterpret_cast<float4*>(d + 2 * AP) =
+                make_float4(v[u][0].z, v[u][1].z, v[u][2].z, v[u][3].z);
+            *reinterpret_cast<float4*>(d + 3 * AP) =
+                make_float4(v[u][0].w, v[u][1].w, v[u][2].w, v[u][3].w);
+          }
+        }
+      };
+
+      bool ok = true;
+      for (int j = 0; j < kStgSlots && a_issued < nsteps; ++j) issue_staging();
+      for (s = 0; s < nsteps; ++s) {
+        const int slot = s % ST;
+        if (s >= ST) {
+          const uint32_t par = (uint32_t)((s / ST) & 1) ^ 1u;
+          ok = __all_sync(FULL, bounded_wait(ptx::smem_addr(&bb->empty[slot]), par, abort_w,
+                                             p.status, kDevTimeoutEmpty, p.timeout_ns));
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = ptx::smem_addr(&bb->fullB[slot]);
+          ptx::mbar_arrive_expect_tx(fb, TMA_BYTES);
+          ptx::tma_load_3d(ptx::smem_addr(Bs + slot * B_ST), &tmapB, cb.n0, cb.k * BK, cb.bi, fb);
+        }
+        ++b_issued;
+        const int j = s % kStgSlots;
+        ok = __all_sync(FULL, bounded_wait(ptx::smem_addr(&staged[j]),
+                                           (uint32_t)((s / kStgSlots) & 1), abort_w, p.status,
+                                           kDevTimeoutFull, p.timeout_ns));
+        if (!ok) break;
+        transpose_slot(Stg + j * (BM * BK), As + slot * A_ST);
+        ptx::mbar_arrive(ptx::smem_addr(&bb->fullA[slot]));
+        // every lane's loads from staging slot j are complete (their values
+        // were stored above): the slot may be refilled by the async proxy
+        __syncwarp();
+        if (a_issued < nsteps) {
+          ptx::fence_proxy_async_shared();
+          issue_staging();
+        }
+        cur_next(cb);
+      }
+      if (!ok && lane == 0) {
+        // abandoned: wait (bounded) for this warp's TMAs still in flight --
+        // the staging slices of steps s .. a_issued - 1 and the B tiles of
+        // the last ST steps issued -- so nothing lands after the CTA is gone
+        const uint64_t t0 = ptx::global_ns();
+        const long long bound = cleanup_bound_ns(p.timeout_ns);
+        for (int t = s; t < a_issued; ++t) {
+          const uint32_t fa = ptx::smem_addr(&staged[t % kStgSlots]);
+          while (!ptx::mbar_try_wait(fa, (uint32_t)((t / kStgSlots) & 1)))
+            if ((long long)(ptx::global_ns() - t0) > bound) break;
+        }
+        for (int t = b_issued - 1; t >= 0 && t >= b_issued - ST; --t) {
+          const uint32_t fb = ptx::smem_addr(&bb->fullB[t % ST]);
+          while (!ptx::mbar_try_wait(fb, (uint32_t)((t / ST) & 1)))
+            if ((long long)(ptx::global_ns() - t0) > bound) break;
+        }
+      }
+      return;
+    }
+  }
 
   // ---- lane geometry --------------------------------------------------------
   const int warp_m = warp / WARPS_N, warp_n = warp % WARPS_N;
@@ -263,7 +431,9 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
       l_brow = Bg + (long long)l_bi * p.sB + (l_n_inside ? (long long)(l_n0 + a_m) * ldb : 0);
   };
   if (npieces > 0) set_load_piece(0);
-  int issued = 0;
+  // steps whose copies this thread has issued (kARowStg: the producer warp
+  // issues every copy, so the FMA warps start with all of them "issued")
+  int issued = kStg ? nsteps : 0;
 
   // Issue the copies of the next step into its ring slot, then advance the
   // cursor. Returns false on abort.
@@ -369,7 +539,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
   auto test_full = [&](int step) -> bool {
     const int slot = step % ST;
     const uint32_t par = (uint32_t)((step / ST) & 1);
-    const bool a = kUsesCp ? ptx::mbar_try_wait(ptx::smem_addr(&bb->fullA[slot]), par) : true;
+    const bool a = kWaitA ? ptx::mbar_try_wait(ptx::smem_addr(&bb->fullA[slot]), par) : true;
     const bool b2 = kUsesTma ? ptx::mbar_try_wait(ptx::smem_addr(&bb->fullB[slot]), par) : true;
     return a && b2;
   };
@@ -380,7 +550,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     if (!ready) {
       const int slot = step % ST;
       const uint32_t par = (uint32_t)((step / ST) & 1);
-      if (kUsesCp)
+      if (kWaitA)
         ok = bounded_wait(ptx::smem_addr(&bb->fullA[slot]), par, abort_w, p.status,
                           kDevTimeoutFull, p.timeout_ns);
       if (kUsesTma && ok)
@@ -696,7 +866,7 @@ __global__ void __launch_bounds__(Cfg::S.NT, Cfg::S.MINB)
     // the tiles it issued and nobody consumed, so nothing lands in shared
     // memory after the CTA is gone.
     ptx::cp_async_wait_all();
-    if (kUsesTma && tid == 0) {
+    if (kUsesTma && !kStg && tid == 0) {
       const uint64_t t0 = ptx::global_ns();
       for (int s = issued - 1; s >= 0 && s >= issued - ST; --s) {
         const uint32_t fb = ptx::smem_addr(&bb->fullB[s % ST]);

@@ -10,20 +10,32 @@
 namespace sgemm_gb300 {
 
 // kAll: instantiate every operand-layout variant (3 x 3); otherwise only the
-// row-major ones (A transposed on store; B by TMA or by copy).
+// row-major ones (A transposed on store; B by TMA or by copy). Configurations
+// that pass stg_eligible also get the staged-A variant (kARowStg, B by TMA),
+// with its own shared-memory size and one more warp.
 template <class Cfg, bool kAll>
 struct Launcher {
   static constexpr int kSmem = kernel_smem_bytes<Cfg>();
+  static constexpr bool kStgOk = stg_eligible(Cfg::S);
+  static constexpr int kSmemStg = kStgOk ? kernel_smem_bytes_stg<Cfg>() : 0;
+
+  template <int AL>
+  static constexpr int smem_of() {
+    return AL == kARowStg ? kSmemStg : kSmem;
+  }
 
   template <int AL, int BL>
   static cudaError_t attr() {
     return cudaFuncSetAttribute(ffma_sgemm_kernel<Cfg, AL, BL>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_of<AL>());
   }
 
   static cudaError_t set_attributes() {
     cudaError_t e = attr<kARow, kBRowTma>();
     if (e == cudaSuccess) e = attr<kARow, kBRowCp>();
+    if constexpr (kStgOk) {
+      if (e == cudaSuccess) e = attr<kARowStg, kBRowTma>();
+    }
     if constexpr (kAll) {
       if (e == cudaSuccess) e = attr<kARow, kBT>();
       if (e == cudaSuccess) e = attr<kATTma, kBRowTma>();
@@ -42,11 +54,23 @@ struct Launcher {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         blocks, ffma_sgemm_kernel<Cfg, kARow, kBRowTma>, Cfg::S.NT, kSmem);
   }
+  // the staged-A variant (its own size and thread count)
+  static cudaError_t occupancy_stg(int* blocks) {
+    if constexpr (kStgOk) {
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          blocks, ffma_sgemm_kernel<Cfg, kARowStg, kBRowTma>, kernel_threads<Cfg, kARowStg>(),
+          kSmemStg);
+    } else {
+      *blocks = 0;
+      return cudaSuccess;
+    }
+  }
 
   template <int AL, int BL>
   static cudaError_t go(int grid, const KernelParams& p, const CUtensorMap* ma,
                         const CUtensorMap* mb, cudaStream_t stream) {
-    ffma_sgemm_kernel<Cfg, AL, BL><<<grid, Cfg::S.NT, kSmem, stream>>>(p, *ma, *mb);
+    ffma_sgemm_kernel<Cfg, AL, BL>
+        <<<grid, kernel_threads<Cfg, AL>(), smem_of<AL>(), stream>>>(p, *ma, *mb);
     return cudaGetLastError();
   }
 
@@ -54,6 +78,9 @@ struct Launcher {
                             const CUtensorMap* ma, const CUtensorMap* mb, cudaStream_t stream) {
     if (al == kARow && bl == kBRowTma) return go<kARow, kBRowTma>(grid, p, ma, mb, stream);
     if (al == kARow && bl == kBRowCp) return go<kARow, kBRowCp>(grid, p, ma, mb, stream);
+    if constexpr (kStgOk) {
+      if (al == kARowStg && bl == kBRowTma) return go<kARowStg, kBRowTma>(grid, p, ma, mb, stream);
+    }
     if constexpr (kAll) {
       if (al == kARow && bl == kBT) return go<kARow, kBT>(grid, p, ma, mb, stream);
       if (al == kATTma && bl == kBRowTma) return go<kATTma, kBRowTma>(grid, p, ma, mb, stream);
@@ -67,7 +94,8 @@ struct Launcher {
   }
 
   static ConfigEntry entry() {
-    return ConfigEntry{Cfg::name, Cfg::S, kSmem, kAll, &set_attributes, &occupancy, &launch};
+    return ConfigEntry{Cfg::name, Cfg::S,      kSmem,   kAll, &set_attributes,
+                       &occupancy, &launch, kStgOk, &occupancy_stg};
   }
 };
 

@@ -67,6 +67,37 @@ constexpr int smem_bytes(const TileShape& s) {
   return 1024 + s.STAGES * (a_stage_floats(s) + b_stage_floats(s)) * 4 + s.STAGES * 3 * 8 + 16;
 }
 
+// Row-major A through a staging ring (ALoad kARowStg in ffma_sgemm.cuh): one
+// TMA box of BM rows x 32 k per k-slice lands, 128-byte swizzled, in one of
+// kStgSlots staging slots, and one extra producer warp transposes it into the
+// padded As[k][m] of the ring. The slots (and one mbarrier each) come on top
+// of the ring, which keeps the configuration's depth or gives up stages until
+// everything fits.
+constexpr int kStgSlots = 2;
+constexpr int stg_smem_bytes(const TileShape& s, int stages) {
+  return 1024 + stages * (a_stage_floats(s) + b_stage_floats(s)) * 4 +
+         kStgSlots * s.BM * s.BK * 4 + stages * 3 * 8 + 16 + kStgSlots * 8;
+}
+constexpr bool stg_fits(const TileShape& s, int stages) {
+  return stg_smem_bytes(s, stages) <= kMaxSmemPerCta &&
+         s.MINB * (stg_smem_bytes(s, stages) + 1024) <= 228 * 1024;
+}
+constexpr int stg_ring_stages(const TileShape& s) {
+  int st = s.STAGES;
+  while (st > 3 && !stg_fits(s, st)) --st;
+  return st;
+}
+// A configuration is built with the staged variant when its slices are 32
+// wide (one 128-byte swizzle span per row), its tile rows fit one TMA box, the
+// ring keeps at least three stages beside the staging slots, and a lane of at
+// most 64 accumulators leaves room for the extra warp: the register cap
+// 65536 / ((NT + 32) * MINB) stays at 200 or more (the 64-accumulator kernels
+// use about 190).
+constexpr bool stg_eligible(const TileShape& s) {
+  return s.BK == 32 && s.BM % 32 == 0 && s.BM <= kTmaMaxBox && stg_fits(s, stg_ring_stages(s)) &&
+         acc_per_thread(s) <= 64 && (s.NT + kWarp) * s.MINB * 200 <= 65536;
+}
+
 // Every assumption of the kernel in ffma_sgemm.cuh, in the order the kernel
 // relies on them. Returns 0 when legal, else the number of the first failed
 // rule (so a test can tell which rule rejected a tuple).

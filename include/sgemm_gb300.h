@@ -264,6 +264,25 @@ int sgemm_config_info(int id, char* name, int len, int* params);
 int sgemm_force_config(int id);
 
 /*
+ * How row-major A reaches shared memory in later calls (process-wide).
+ * The staged variant: where the configuration is built with it (32-wide
+ * k-slices, at most 64 accumulators per lane), B arrives by TMA and A is
+ * 16-byte aligned with lda (and, batched, the matrix stride) a multiple of 4,
+ * one TMA box per k-slice copies A as it is stored into a staging slot and
+ * one extra producer warp transposes it into the padded As[k][m], so the FMA
+ * warps issue no copies. Otherwise every thread issues the transposing
+ * 4-byte copy ("Vectorized Memory Access: 128-bit Loads and Stores", section
+ * "Why As Has To Be Transposed"; the pages copy with the FMA threads).
+ * on = 1 (the default): the staged variant where allowed and each CTA runs
+ * at least 8 k-slices on average (below that its extra step of latency
+ * costs more than it saves); 2: wherever allowed, whatever the size; 0:
+ * never. Both fill the same As[k][m] and sum in the same order, so results
+ * are bit-identical. Returns the previous setting, or
+ * SGEMM_ERR_INVALID_VALUE (nothing changed) for another value.
+ */
+int sgemm_set_staged_a(int on);
+
+/*
  * 1 when tile configuration `id` is built for every operand layout (op(A),
  * op(B) in {N, T}; sgemm_ex and sgemm_strided_batched can use it), 0 when
  * only for row-major A and B, SGEMM_ERR_INVALID_VALUE for an unknown id.

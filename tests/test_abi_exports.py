@@ -63,6 +63,9 @@ def test_validation_happens_before_any_device_call():
     assert binding.sgemm_3xtf32_set_kernel_form(binding.SGEMM_X3_PAIR) == binding.SGEMM_X3_SINGLE
     assert binding.sgemm_host_set_pipeline(-1, 0, 0, 0) == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_host_set_pipeline(0, 0, 0, 9) == binding.SGEMM_ERR_INVALID_VALUE
+    for bad in (-1, 3):
+        assert binding.sgemm_set_staged_a(bad) == binding.SGEMM_ERR_INVALID_VALUE
+    assert binding.sgemm_set_staged_a(1) == 1
     for k in (0, 1, 6, 9):
         assert binding.sgemm_ladder(k, 4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, None) == binding.SGEMM_ERR_INVALID_VALUE
 
