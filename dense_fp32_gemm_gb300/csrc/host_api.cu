@@ -101,6 +101,28 @@ int chunk_bounds(int M, int N, int K, const Pipeline& pp, int* kb) {
   return n;
 }
 
+// Row panels of the last chunk for `panels` panels of M rows: bounds
+// 0 = r[0] < ... < r[n] = M, returns n. The panel copied back last is the
+// only copy nothing hides, so it is short: about M / (4 panels) rows (measured
+// on GB300 at 4096^3: 2.34 ms against 2.39 for four equal panels); the others
+// share the rest equally (all multiples of 128 rows but the end).
+int panel_bounds(int M, int panels, int* r) {
+  auto r128 = [](long long x) { return (int)((x + 127) / 128 * 128); };
+  int n = 0;
+  r[0] = 0;
+  if (panels <= 1) {
+    r[++n] = M;
+    return n;
+  }
+  int last = r128((long long)M / (4 * panels));
+  if (last >= M / 2) last = 0;
+  const int body = M - last, nb = last > 0 ? panels - 1 : panels;
+  const int rows = r128((body + nb - 1) / nb);
+  for (int r0 = 0; r0 < body; r0 += rows) r[++n] = r0 + rows < body ? r0 + rows : body;
+  if (last > 0) r[++n] = M;
+  return n;
+}
+
 struct HostCtx {
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
@@ -279,14 +301,15 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
           cudaEventRecord(c->chunk[i], c->h2d) != cudaSuccess)
         return fail();
     }
-    // row panels of the last chunk
+    // row panels of the last chunk: [r_0, r_1), [r_1, r_2), ...
     const int panels = M >= 512 * g_pipe.panels ? g_pipe.panels : (M >= 1024 ? M / 512 : 1);
-    const int rows = ((M + panels - 1) / panels + 127) / 128 * 128;
+    int pr[kMaxPanels + 1];
+    const int np = panel_bounds(M, panels, pr);
     // the incoming C, one row panel at a time: panel p's add waits only for
     // its own rows
     if (beta != 0.f) {
-      for (int pi = 0, r0 = 0; r0 < M; ++pi, r0 += rows) {
-        const int r1 = (r0 + rows < M) ? r0 + rows : M;
+      for (int pi = 0; pi < np; ++pi) {
+        const int r0 = pr[pi], r1 = pr[pi + 1];
         if (cudaMemcpy2DAsync(c->dC0 + (size_t)r0 * N, row_c, C + (size_t)r0 * ldc, pitch_c, row_c,
                               r1 - r0, cudaMemcpyHostToDevice, c->h2d) != cudaSuccess ||
             cudaEventRecord(c->c_in_panel[pi], c->h2d) != cudaSuccess)
@@ -302,8 +325,8 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
     // last chunk in row panels, each copied back as soon as it is final
     const int k0 = kb[nk - 1], kl = K - k0;
     if (cudaStreamWaitEvent(user, c->chunk[nk - 1], 0) != cudaSuccess) return fail();
-    for (int pi = 0, r0 = 0; r0 < M; ++pi, r0 += rows) {
-      const int r1 = (r0 + rows < M) ? r0 + rows : M;
+    for (int pi = 0; pi < np; ++pi) {
+      const int r0 = pr[pi], r1 = pr[pi + 1];
       float* dCp = c->dC + (size_t)r0 * N;
       st = library_ffma(r1 - r0, N, kl, alpha, c->dA + (size_t)r0 * K + k0, K,
                         c->dB + (size_t)k0 * N, N, nk == 1 ? 0.f : 1.f, dCp, N, user);
