@@ -175,25 +175,26 @@ __global__ void pack_a_kernel(int M, int K, const float* __restrict__ A, long lo
 }
 
 // B (K x N, ldb) -> B^T (N x K, ldw), through 32 x 32 shared-memory tiles so
-// that both the reads and the writes are coalesced. Tile columns over
-// blockIdx.x, tile rows over blockIdx.y strided by gridDim.y (any K).
+// that both the reads and the writes are coalesced: one tile per block, tile
+// column blockIdx.x, tile row k_base / 32 + blockIdx.y (the host launches one
+// grid per 65535 tile rows). Bounds are compared as remaining extents, so no
+// index passes K or N even for K, N near 2^31. (A grid-stride form of this
+// kernel, looping over tile rows in 64-bit indices, took 43 us instead of
+// 23 us at 4096 x 4096 on GB300.)
 __global__ void transpose_b_kernel(int K, int N, const float* __restrict__ B, long long ldb,
-                                   float* __restrict__ bt, long long ldw) {
+                                   float* __restrict__ bt, long long ldw, int k_base) {
   __shared__ float tile[32][33];
-  const long long n0 = (long long)blockIdx.x * 32;
+  const int n0 = blockIdx.x * 32, k0 = k_base + blockIdx.y * 32;
+  const int kn = K - k0, nn = N - n0;             // both > 0
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
-  for (long long k0 = (long long)blockIdx.y * 32; k0 < K; k0 += (long long)gridDim.y * 32) {
-    for (int j = 0; j < 32; j += 8) {
-      const long long k = k0 + ty + j, n = n0 + tx;
-      tile[ty + j][tx] = (k < K && n < N) ? B[k * ldb + n] : 0.f;
-    }
-    __syncthreads();
-    for (int j = 0; j < 32; j += 8) {
-      const long long n = n0 + ty + j, k = k0 + tx;
-      if (n < N && k < K) bt[n * ldw + k] = tile[tx][ty + j];
-    }
-    __syncthreads();  // the tile is rewritten by the next row of tiles
-  }
+#pragma unroll
+  for (int j = 0; j < 32; j += 8)
+    tile[ty + j][tx] =
+        (ty + j < kn && tx < nn) ? B[(long long)(k0 + ty + j) * ldb + (n0 + tx)] : 0.f;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 32; j += 8)
+    if (ty + j < nn && tx < kn) bt[(long long)(n0 + ty + j) * ldw + (k0 + tx)] = tile[tx][ty + j];
 }
 
 // The residual x_lo of four raw values.
@@ -830,10 +831,12 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
 
   // 1. B^T (and, when needed, an aligned copy of A)
   {
-    const int ktiles = ceil_div_nn(K, 32);
-    dim3 grid((unsigned)ceil_div_nn(N, 32), (unsigned)(ktiles < 65535 ? ktiles : 65535)),
-        block(32, 8);
-    x3::transpose_b_kernel<<<grid, block, 0, stream>>>(K, N, B, ldb, bt, Kp);
+    constexpr long long kRowsPerGrid = 65535LL * 32;  // tile rows of one grid (gridDim.y)
+    for (long long kb = 0; kb < K; kb += kRowsPerGrid) {
+      const int ktiles = ceil_div_nn((int)(K - kb < kRowsPerGrid ? K - kb : kRowsPerGrid), 32);
+      dim3 grid((unsigned)ceil_div_nn(N, 32), (unsigned)ktiles), block(32, 8);
+      x3::transpose_b_kernel<<<grid, block, 0, stream>>>(K, N, B, ldb, bt, Kp, (int)kb);
+    }
     if (!a_direct) {
       const int bx = (K + 255) / 256 < 8 ? (K + 255) / 256 : 8;
       const int by = M < 65535 ? M : 65535;
