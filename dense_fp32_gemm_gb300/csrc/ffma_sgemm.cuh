@@ -103,7 +103,7 @@ enum BLoad : int { kBRowTma = 0, kBRowCp = 1, kBT = 2 };
 template <int ST>
 struct BarrierBlock {
   uint64_t fullA[ST];   // NT cp.async arrivals: this thread's copies landed (kARowStg:
-                        // one arrival per producer lane once it has stored its part)
+                        // one arrival by the producer warp once all its lanes have stored)
   uint64_t fullB[ST];   // one expect_tx arrival + the TMA transaction bytes of the stage
   uint64_t empty[ST];   // one arrival per warp: the slot may be refilled
   uint64_t sync;        // CTA-wide rendezvous with a bounded wait
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kernel_threads<Cfg, AL>(), Cfg::S.MINB)
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&bb->fullA[s]), kStg ? kWarp : NT);
+      ptx::mbar_init(ptx::smem_addr(&bb->fullA[s]), kStg ? 1 : NT);
       ptx::mbar_init(ptx::smem_addr(&bb->fullB[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&bb->empty[s]), NT / 32);
     }
@@ -359,10 +359,11 @@ __global__ void __launch_bounds__(kernel_threads<Cfg, AL>(), Cfg::S.MINB)
                                            kDevTimeoutFull, p.timeout_ns));
         if (!ok) break;
         transpose_slot(Stg + j * (BM * BK), As + slot * A_ST);
-        ptx::mbar_arrive(ptx::smem_addr(&bb->fullA[slot]));
+        // the warp's stores are ordered before lane 0's release on fullA; and
         // every lane's loads from staging slot j are complete (their values
-        // were stored above): the slot may be refilled by the async proxy
+        // were stored above), so the slot may be refilled by the async proxy
         __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bb->fullA[slot]));
         if (a_issued < nsteps) {
           ptx::fence_proxy_async_shared();
           issue_staging();
