@@ -25,6 +25,8 @@
 
 namespace sgemm_gb300 {
 
+bool library_staged_a_wanted(bool built, int occ, int occ_staged, const Schedule& s);
+
 // The kernel for very small problems (tiny.cu).
 bool tiny_wanted(int M, int N, int K);
 cudaError_t tiny_launch(int dev, int M, int N, int K, float alpha, const float* A, long long lda,
@@ -306,11 +308,8 @@ int run_ffma(int opA, int opB, int M, int N, int K, float alpha, const float* A,
   // 128-byte swizzled), and each CTA runs enough k-slices to cover the extra
   // step of latency the staging adds before the first FMA (measured on
   // GB300: 4 k-slices per CTA at 512^3 lose 5 %, 13 at 1024^3 gain 4 %)
-  const int staged_mode = g_staged_a.load();
-  if (al == kARow && bl == kBRowTma && cfg.staged && staged_mode != 0 &&
-      di->occupancy_staged[id] == occ &&
-      (staged_mode == 2 ||
-       (long long)sched.tiles * kiters >= (long long)kStagedMinSteps * sched.grid) &&
+  if (al == kARow && bl == kBRowTma &&
+      library_staged_a_wanted(cfg.staged, occ, di->occupancy_staged[id], sched) &&
       ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0) &&
       (single || (sA & 3) == 0) &&
       encode_3d(enc, &map_a, A, K, M, lda, sA, batch, S.BK, S.BM, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -411,6 +410,17 @@ int library_device_sms(int dev, int* sms) {
 void note_last_config(const char* text) { snprintf(g_last_config, sizeof(g_last_config), "%s", text); }
 
 long long library_wait_timeout_ns() { return g_timeout_ns.load(); }
+
+// Whether a row-major problem whose B arrives by TMA takes A through the
+// staging ring (ALoad kARowStg), before the alignment checks: the
+// configuration is built with it at the same residency, and the
+// sgemm_set_staged_a mode allows it (2: always; 1: when each CTA runs at
+// least kStagedMinSteps k-slices). Shared by sgemm() and sgemm_noalloc.
+bool library_staged_a_wanted(bool built, int occ, int occ_staged, const Schedule& s) {
+  const int mode = g_staged_a.load();
+  return built && mode != 0 && occ_staged == occ &&
+         (mode == 2 || (long long)s.tiles * s.kiters >= (long long)kStagedMinSteps * s.grid);
+}
 
 // The FFMA path on device matrices (row-major, arguments already checked).
 int library_ffma(int M, int N, int K, float alpha, const float* A, int lda, const float* B,

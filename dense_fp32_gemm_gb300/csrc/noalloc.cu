@@ -55,6 +55,7 @@ namespace sgemm_gb300 {
 
 // Provided by api.cu.
 long long library_wait_timeout_ns();
+bool library_staged_a_wanted(bool built, int occ, int occ_staged, const Schedule& s);
 
 // The kernel for very small problems (tiny.cu); it needs no scratch.
 bool tiny_wanted(int M, int N, int K);
@@ -83,6 +84,7 @@ struct NoAllocDevice {
   bool ready;
   int sms;
   int occupancy[kNoAllocNumConfigs];
+  int occupancy_staged[kNoAllocNumConfigs];  // staged-A variant (0: not built)
   unsigned char* base;  // device address of g_noalloc_scratch on this device
   uint32_t epoch;
 };
@@ -123,6 +125,13 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
         return SGEMM_ERR_LAUNCH;
       }
       d.occupancy[c] = blocks;
+      blocks = 0;
+      if (kNoAllocConfigs[c]->staged &&
+          kNoAllocConfigs[c]->occupancy_staged(&blocks) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+      }
+      d.occupancy_staged[c] = blocks;
     }
     d.base = static_cast<unsigned char*>(ptr);
     d.epoch = 0;
@@ -216,8 +225,9 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   CUtensorMap map_a, map_b;
   std::memset(&map_a, 0, sizeof(map_a));
   std::memset(&map_b, 0, sizeof(map_b));
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if (tma) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = noalloc_encoder();
+    enc = noalloc_encoder();
     tma = false;
     if (enc != nullptr) {
       // one matrix: a 3-D map with a batch extent of 1
@@ -237,6 +247,23 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   if (occ < 1) return SGEMM_ERR_LAUNCH;
   const Schedule sched = make_schedule(tiles_m, tiles_n, ceil_div_nn(K, S.BK), d->sms * occ,
                                        choose_policy(M, N, K));
+  // row-major A through the staging ring, under the same rule as sgemm() (the
+  // same kernel variant, so the same bits): a K x M box of 32 x BM, 128-byte
+  // swizzled
+  int al = kARow;
+  if (tma && enc != nullptr &&
+      library_staged_a_wanted(cfg.staged, occ, d->occupancy_staged[id], sched) &&
+      ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0)) {
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)M, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)lda * 4,
+                             (cuuint64_t)(((long long)lda * (M > 0 ? M : 1) * 4 + 15) / 16 * 16)};
+    cuuint32_t box[3] = {(cuuint32_t)S.BK, (cuuint32_t)S.BM, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(A), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      al = kARowStg;
+  }
   const bool split = sched.dp_tiles < sched.tiles;
   const size_t partial_bytes = split ? (size_t)sched.grid * S.BM * S.BN * 4 : 0;
   if ((size_t)sched.grid > kNoAllocMaxFlags ||
@@ -277,7 +304,7 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float* A, in
   p.epoch = d->epoch;
   p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && ((ldc & 3) == 0);
   p.timeout_ns = library_wait_timeout_ns();
-  if (cfg.launch(kARow, tma ? kBRowTma : kBRowCp, sched.grid, p, &map_a, &map_b, stream) !=
+  if (cfg.launch(al, tma ? kBRowTma : kBRowCp, sched.grid, p, &map_a, &map_b, stream) !=
       cudaSuccess) {
     cudaGetLastError();
     return SGEMM_ERR_LAUNCH;

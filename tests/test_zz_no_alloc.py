@@ -62,6 +62,21 @@ def test_noalloc_matches_sgemm_twice(w):
         assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_noalloc_follows_the_staged_a_switch(mode):
+    # the same A load mode as sgemm() under every setting of sgemm_set_staged_a
+    # (SPLIT: row-major, TMA-aligned, every tile split; SKINNY: 64 k-slices per CTA)
+    prev = binding.sgemm_set_staged_a(mode)
+    try:
+        for w in (SPLIT, Workload("noalloc_skinny", 4096, 64, 4096, 1.0, 1.0, "uniform", 23)):
+            A, B, C = make_inputs(w)
+            dA, dB = A.to("cuda"), B.to("cuda")
+            ref = _call(binding.sgemm, w, dA, dB, C)
+            assert np.array_equal(_call(binding.sgemm_noalloc, w, dA, dB, C), ref), (mode, w.name)
+    finally:
+        binding.sgemm_set_staged_a(prev)
+
+
 def test_noalloc_allocates_nothing():
     w = SPLIT
     A, B, C = make_inputs(w)
