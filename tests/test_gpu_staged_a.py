@@ -88,6 +88,22 @@ def test_matches_oracle_and_the_copy_path(config, dist, shape, staged):
     assert np.array_equal(got, got_copy, equal_nan=True)
 
 
+@pytest.mark.parametrize("shape", [(1, 64, 1), (5, 7, 5), (255, 33, 31), (257, 100, 32), (64, 1, 65),
+                                   (300, 64, 8), (1, 300, 100)], ids=lambda s: "x".join(map(str, s)))
+def test_edge_shapes(shape, staged):
+    # K below one slice, single rows and columns, ragged tiles: TMA fills what
+    # lies outside A with zeros, and the result is exact on integers
+    M, N, K = shape
+    for cid in ELIGIBLE:
+        w = Workload("stgedge", M, N, K, 1.0, 1.0, "int3", 67, lda=K + (-K) % 4,
+                     ldb=N + (-N) % 4)
+        A, B, C = make_inputs(w)
+        got = H.run_cuda(w, A, B, C, config=cid)
+        assert "a=stg" in binding.sgemm_last_config(), (cid, shape)
+        ref, mag = H.oracle_full(w, A, B, C)
+        H.assert_match(w, H.logical(got, w.M, w.N, w.LDC), ref, mag, what=f"cfg {cid} {shape}")
+
+
 def _last_with(w, cid, offsets):
     A, B, C = make_inputs(w)
     H.run_cuda(w, A, B, C, offsets=offsets, config=cid)
