@@ -324,7 +324,8 @@ SGEMM_X3_SINGLE, SGEMM_X3_PAIR = 1, 2
 X3_FORMS = (SGEMM_X3_PAIR, SGEMM_X3_SINGLE)
 
 
-X3_PLAN_FIELDS = ("form", "bk", "stages", "ctas", "units", "dp_units", "split_units", "kiters")
+X3_PLAN_FIELDS = ("form", "bk", "stages", "ctas", "units", "dp_units", "split_units", "kiters",
+                  "bn")
 
 
 def sgemm_3xtf32_plan(M: int, N: int, K: int, form: int, pairs: int, sms: int):

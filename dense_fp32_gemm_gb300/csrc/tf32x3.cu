@@ -91,36 +91,47 @@ constexpr int kMaxStages = 6;
 // tile, and BK = 32 gives three 64 KB stages (its hand-offs between the CTAs
 // of a pair cost more, so it always takes 32; 16-wide stages measured 158
 // against 265 TFLOP/s at 4096^3).
-template <int BK_, int B_PARTS = 1>
+// BNT: the tile's width in N (BN, or 64 for N <= 64: see make_plan); a
+// narrow tile keeps the configured stage count, up to kMaxStages.
+template <int BK_, int B_PARTS = 1, int BNT = BN>
 struct Slice {
   static constexpr int BK = BK_;
   static_assert(BK == 32 || BK == 16, "k-slice width");
   static constexpr int ROW_BYTES = BK * 4;
   static constexpr int A_BYTES = BM * BK * 4;                      // one of A_hi, A_lo
-  static constexpr int B_BYTES = BN / B_PARTS * BK * 4;            // one of B_hi, B_lo
+  static constexpr int B_BYTES = BNT / B_PARTS * BK * 4;           // one of B_hi, B_lo
   // a stage: [A_hi | A_lo | B_hi | B_lo]; TMA writes the _hi tiles (the raw
   // values), the converter warps the _lo tiles
   static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 / 48 KB, or 64 / 32 KB
-  static constexpr int ST = kStageRegion / STAGE_BYTES;            // 2 / 4, or 3 / 6
+  static constexpr int ST = kStageRegion / STAGE_BYTES < kMaxStages
+                                ? kStageRegion / STAGE_BYTES
+                                : kMaxStages;                      // 2 / 4, or 3 / 6
 };
 static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
                   Slice<32>::ST * Slice<32>::STAGE_BYTES == kStageRegion &&
                   Slice<32, 2>::ST * Slice<32, 2>::STAGE_BYTES == kStageRegion &&
                   Slice<16>::ST <= kMaxStages,
               "every width fills the same stage region");
-constexpr int ACC_COLS = BN;              // one FP32 accumulator: 128 lanes x BN columns
 constexpr int NBUF = 2;                   // accumulators, so the epilogue overlaps the next MMAs
-constexpr int TMEM_COLS = NBUF * ACC_COLS;  // all 512 columns
+// One FP32 accumulator is 128 lanes x BNT columns; NBUF of them (all 512
+// columns for BNT = BN, 128 for the 64-wide tile).
+constexpr int tmem_cols(int bnt) { return NBUF * bnt; }
 // Kernel forms (the values sgemm_3xtf32_set_kernel_form takes): single CTAs;
 // CTA pairs whose even CTA issues M = 256 MMAs over both (cta_group::2),
 // each CTA holding half of every B tile.
 enum Form : int { kSingle = 1, kTwoSmPair = 2 };
+// Stages of a (form, k-slice width, tile width): Slice<>::ST, for the host.
+constexpr int stages_of(int form, int bk, int bnt) {
+  const int stage = 2 * BM * bk * 4 + 2 * (bnt / (form == kTwoSmPair ? 2 : 1)) * bk * 4;
+  return kStageRegion / stage < kMaxStages ? kStageRegion / stage : kMaxStages;
+}
 constexpr int EPI_THREADS = 128;          // warps 2-5
 constexpr int CONV_WARP0 = 6;             // warps 6-9 write the residual tiles
 constexpr int CONV_THREADS = 128;
-constexpr uint32_t IDESC = tc::idesc_tf32(BM, BN);
 constexpr uint32_t IDESC_PAIR = tc::idesc_tf32(2 * BM, BN);  // M = 256 over a CTA pair
 static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
+// the narrow tile of problems with N <= 64
+constexpr int BN_NARROW = 64;
 
 struct Barriers {
   uint64_t full[kMaxStages];   // TMA transaction bytes of one stage (the raw tiles)
@@ -149,7 +160,7 @@ struct Params {
   float* C;
   long long ldc;
   Schedule sched;     // whole tiles, then K-split tiles (schedule.hpp)
-  float* ws;          // grid partial tiles of BM x BN floats, column-major
+  float* ws;          // grid partial tiles of BM x BNT floats, column-major
   uint32_t* flags;    // flags[s] == epoch once slot s's partial is written; reset
                       // to 0 by the owner that reads it
   uint32_t epoch;
@@ -224,7 +235,7 @@ __device__ __forceinline__ bool bounded_wait_cluster(uint32_t bar, uint32_t pari
   return ptx::mbar_try_wait_cluster(bar, parity);
 }
 
-template <int FORM, int BK>
+template <int FORM, int BK, int BNT = BN>
 __global__ void __launch_bounds__(NT, 1)
     gemm_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB) {
@@ -240,7 +251,11 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr bool TWO_SM = FORM == kTwoSmPair;
   constexpr int CL = TWO_SM ? 2 : 1;                // CTAs per cluster
   constexpr int CG = TWO_SM ? 2 : 1;                // cta_group of every tcgen05 instruction
-  using S = Slice<BK, TWO_SM ? 2 : 1>;
+  static_assert(BNT == BN || (!TWO_SM && BNT % 16 == 0 && BNT >= 32), "tile width");
+  using S = Slice<BK, TWO_SM ? 2 : 1, BNT>;
+  constexpr int ACC_COLS = BNT;
+  constexpr int TMEM_COLS = tmem_cols(BNT);
+  constexpr uint32_t IDESC = tc::idesc_tf32(BM, BNT);
   constexpr int ST = S::ST, ROW_BYTES = S::ROW_BYTES;
   constexpr int A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES, STAGE_BYTES = S::STAGE_BYTES;
   constexpr uint16_t kPair = 0x3;  // both CTAs of a cluster of two
@@ -322,7 +337,7 @@ __global__ void __launch_bounds__(NT, 1)
             // this CTA's half of the B tile (N columns 128 * rank ..), into this CTA
             ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN + rank * (BN / 2), fb);
           } else {
-            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN, fb);
+            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BNT, fb);
           }
         }
         if (!ok) break;
@@ -364,7 +379,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
       }
     }
-    // ---- MMA issuer: piece i accumulates into TMEM columns (i % NBUF) * BN.
+    // ---- MMA issuer: piece i accumulates into TMEM columns (i % NBUF) * BNT.
     // In the two-SM form the even CTA issues for the pair.
     if (lane == 0 && (!TWO_SM || rank == 0)) {
       int it = 0;
@@ -503,12 +518,12 @@ __global__ void __launch_bounds__(NT, 1)
                                    abort_w, p.status, kDevTimeoutFull, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::fence_after_sync();
-      float* my_ws = p.ws + (long long)slot * (BM * BN);
+      float* my_ws = p.ws + (long long)slot * (BM * BNT);
       if (is_partial_piece(sc, pc)) {
         // publish the partial tile (column-major: a warp writes 128 bytes
         // per column)
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = 0; c0 < BNT; c0 += 16) {
           uint32_t v[16];
           tc::tmem_ld16(acc + (uint32_t)c0, v);
           tc::tmem_wait_ld();
@@ -552,7 +567,7 @@ __global__ void __launch_bounds__(NT, 1)
         float* stage = epi + quarter * EPI_WARP_FLOATS;
         const int sub_r = lane >> 3, sub_c = (lane & 7) * 4;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = 0; c0 < BNT; c0 += 32) {
           uint32_t v[32];
           tc::tmem_ld16(acc + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
           tc::tmem_ld16(acc + (uint32_t)(c0 + 16), *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
@@ -562,7 +577,7 @@ __global__ void __launch_bounds__(NT, 1)
           for (int e = 0; e < 32; ++e) a[e] = __uint_as_float(v[e]);
           // partials of schedule units b+1 .. b+nc (same rank), in that order
           for (int c = 1; c <= nc; ++c) {
-            const float* src = p.ws + (long long)((b + c) * CL + rank) * (BM * BN);
+            const float* src = p.ws + (long long)((b + c) * CL + rank) * (BM * BNT);
 #pragma unroll
             for (int e = 0; e < 32; ++e) a[e] += __ldcg(src + (c0 + e) * BM + r);
           }
@@ -572,7 +587,7 @@ __global__ void __launch_bounds__(NT, 1)
             *reinterpret_cast<float4*>(stage + lane * EPI_PITCH + q * 4) =
                 make_float4(a[q * 4], a[q * 4 + 1], a[q * 4 + 2], a[q * 4 + 3]);
           __syncwarp();
-          const int col = tn * BN + c0 + sub_c;
+          const int col = tn * BNT + c0 + sub_c;
           const int row0 = tm * BM + quarter * 32 + sub_r;  // + 4 g for access g
           const bool full = vec && col + 3 < p.N;
           // every read of C is issued before any write, so the reads overlap
@@ -662,20 +677,30 @@ bool g_encode_tried = false;
 // requested form, `pairs` how many CTA pairs the device keeps resident (0:
 // none), `sms` the SM count.
 struct Plan {
-  int form, bk, kiters;
+  int form, bk, kiters, bn;
   Schedule sched;
 };
 Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   Plan pl{};
   pl.form = (want != kSingle && pairs > 0) ? want : (int)kSingle;
+  // N <= 64: 64-wide tiles (single CTAs), so that the MMAs compute no
+  // columns beyond N -- a 256-wide tile would spend three quarters of its
+  // tensor-core work on them (16384 x 64 x 4096: 89.7 us against 149)
+  pl.bn = N <= BN_NARROW ? BN_NARROW : BN;
+  if (pl.bn != BN) pl.form = kSingle;
   // schedule: whole tiles, then the last one to two waves split along K. In
   // the pair form a schedule unit is two vertically adjacent tiles (a tile
   // row pair), handed to one cluster.
-  const int tiles_m = ceil_div_nn(M, BM), tiles_n = ceil_div_nn(N, BN);
+  const int tiles_m = ceil_div_nn(M, BM), tiles_n = ceil_div_nn(N, pl.bn);
   // the k-slice width (see Slice). The two-SM form always takes 32: its
   // stages halve the per-stage hand-offs between the CTAs of a pair
   // (measured at 4096^3: 265 against 158 TFLOP/s with 16).
-  auto slice_width = [K](int f) { return (f == kTwoSmPair || K < 1024) ? 32 : 16; };
+  // 64-wide tiles also take 32: their stages carry a quarter of the MMA work,
+  // so the per-stage hand-offs dominate (measured at 16384 x 64 x 4096: 89.7
+  // against 106.8 us with 16-wide slices)
+  auto slice_width = [K, &pl](int f) {
+    return (f == kTwoSmPair || K < 1024 || pl.bn != BN) ? 32 : 16;
+  };
   pl.bk = slice_width(pl.form);
   pl.kiters = ceil_div_nn(K, pl.bk);
   if (pl.form != kSingle) {
@@ -770,6 +795,10 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
       using namespace x3;
       if (cudaFuncSetAttribute(gemm_kernel<kSingle, 16>, attr, SMEM_BYTES) != cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kSingle, 32>, attr, SMEM_BYTES) != cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kSingle, 16, BN_NARROW>, attr, SMEM_BYTES) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kSingle, 32, BN_NARROW>, attr, SMEM_BYTES) !=
+              cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kTwoSmPair, 32>, attr, SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
@@ -805,7 +834,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   if (enc == nullptr) return SGEMM_ERR_LAUNCH;
 
   const x3::Plan plan = x3::make_plan(M, N, K, x3::g_form.load(), pairs, sms);
-  const int form = plan.form, bk = plan.bk, kiters = plan.kiters;
+  const int form = plan.form, bk = plan.bk, kiters = plan.kiters, bn = plan.bn;
   const Schedule& sched = plan.sched;
   const int CL = form == x3::kSingle ? 1 : 2;
   const bool split = sched.dp_tiles < sched.tiles;
@@ -817,7 +846,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   const bool a_direct = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((lda & 3) == 0);
   const size_t bt_floats = (size_t)N * Kp;
   const size_t a_floats = a_direct ? 0 : (size_t)M * Kp;
-  const size_t partial_floats = split ? (size_t)ctas * x3::BM * x3::BN : 0;
+  const size_t partial_floats = split ? (size_t)ctas * x3::BM * bn : 0;
   float* ws = nullptr;
   int* status = nullptr;
   uint32_t* flags = nullptr;
@@ -849,7 +878,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   CUtensorMap mA, mB;
   if (!x3::encode_k_major(enc, &mA, a_direct ? A : a_copy, M, K, a_direct ? (long long)lda : Kp,
                           x3::BM, bk) ||
-      !x3::encode_k_major(enc, &mB, bt, N, K, Kp, x3::BN / CL, bk))
+      !x3::encode_k_major(enc, &mB, bt, N, K, Kp, bn / CL, bk))
     return SGEMM_ERR_LAUNCH;
   x3::Params p;
   p.M = M;
@@ -866,7 +895,14 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   p.status = status;
   p.timeout_ns = library_wait_timeout_ns();
   if (CL == 1) {
-    if (bk == 16)
+    using x3::BN_NARROW;
+    if (bn == BN_NARROW && bk == 16)
+      x3::gemm_kernel<x3::kSingle, 16, BN_NARROW>
+          <<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
+    else if (bn == BN_NARROW)
+      x3::gemm_kernel<x3::kSingle, 32, BN_NARROW>
+          <<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
+    else if (bk == 16)
       x3::gemm_kernel<x3::kSingle, 16><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
     else
       x3::gemm_kernel<x3::kSingle, 32><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
@@ -894,7 +930,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   char text[160];
   snprintf(text, sizeof(text),
            "3xtf32_tcgen05_%dx%dx%d_s%d cluster=%d%s grid=%d units=%d dp=%d split=%d kiters=%d%s",
-           x3::BM, x3::BN, bk, (form == x3::kTwoSmPair ? 96 : 64) / bk, CL,
+           x3::BM, bn, bk, x3::stages_of(form, bk, bn), CL,
            form == x3::kTwoSmPair ? " pair=2sm" : "",
            ctas, sched.grid, sched.dp_tiles,
            sched.tiles - sched.dp_tiles, kiters, a_direct ? "" : " a=copied");
@@ -912,12 +948,13 @@ SGEMM_API int sgemm_3xtf32_plan(int M, int N, int K, int form, int pairs, int sm
   const x3::Plan pl = x3::make_plan(M, N, K, form, pairs, sms);
   out[0] = pl.form;
   out[1] = pl.bk;
-  out[2] = (pl.form == x3::kTwoSmPair ? 96 : 64) / pl.bk;   // stages
+  out[2] = x3::stages_of(pl.form, pl.bk, pl.bn);             // stages
   out[3] = pl.sched.grid * (pl.form == x3::kSingle ? 1 : 2);  // CTAs
   out[4] = pl.sched.grid;                                    // schedule units
   out[5] = pl.sched.dp_tiles;
   out[6] = pl.sched.tiles - pl.sched.dp_tiles;
   out[7] = pl.kiters;
+  out[8] = pl.bn;
   return SGEMM_OK;
 }
 

@@ -131,10 +131,11 @@ int sgemm_3xtf32_set_kernel_form(int form);
  * The plan sgemm_3xtf32 follows for an M x N x K problem (host arithmetic
  * only, no device needed): `form` is the requested kernel form, `pairs` how
  * many CTA pairs the device keeps resident (0: none), `sms` its SM count.
- * out = {form that runs, k-slice width, stages, CTAs, schedule units (a CTA
- * pair each in the pair forms), whole-tile units, K-split units, k-slices}.
- * The pair form falls back to single CTAs when pairs == 0 or when every tile
- * would be split along K. Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM unless
+ * out (9 ints) = {form that runs, k-slice width, stages, CTAs, schedule
+ * units (a CTA pair each in the pair forms), whole-tile units, K-split units,
+ * k-slices, tile width in N}. The pair form falls back to single CTAs when
+ * pairs == 0 or when every tile would be split along K; N <= 64 takes 64-wide
+ * tiles (single CTAs) instead of 256-wide ones. Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM unless
  * M, N, K >= 1 (only such problems launch the GEMM kernel), or
  * SGEMM_ERR_INVALID_VALUE for another form, pairs < 0, sms < 1 or a NULL out.
  * The pages are silent (no tensor-core kernel, one CTA per tile).

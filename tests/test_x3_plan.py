@@ -3,8 +3,9 @@ runs, the k-slice width, the stages and the persistent schedule. The pair
 form falls back to single CTAs when the device keeps no CTA pairs resident or
 when every tile would be split along K; the two-SM form always takes 32-wide
 slices (three stages of half B tiles), single CTAs 16 from K = 1024 up and 32
-below. The GB300 figures (152 SMs, 76 resident pairs) are the ones the GPU
-runs report in sgemm_last_config()."""
+below; N <= 64 takes 64-wide tiles on single CTAs with 32-wide slices. The
+GB300 figures (152 SMs, 76 resident pairs) are the ones the GPU runs report in
+sgemm_last_config()."""
 import pytest
 
 from dense_fp32_gemm_gb300 import binding
@@ -22,7 +23,7 @@ def plan(M, N, K, form, pairs=PAIRS, sms=SMS):
 def test_square4096_in_each_form():
     # 32 x 16 tiles of 128 x 256: 256 tile pairs on 76 clusters
     p = plan(4096, 4096, 4096, PAIR)
-    assert (p["form"], p["bk"], p["stages"], p["ctas"], p["units"]) == (PAIR, 32, 3, 152, 76)
+    assert (p["form"], p["bk"], p["stages"], p["ctas"], p["units"], p["bn"]) == (PAIR, 32, 3, 152, 76, 256)
     assert (p["dp_units"], p["split_units"], p["kiters"]) == (152, 104, 128)
     p = plan(4096, 4096, 4096, SINGLE)
     assert (p["form"], p["bk"], p["stages"], p["ctas"], p["units"]) == (SINGLE, 16, 4, 152, 152)
@@ -59,7 +60,7 @@ def test_schedule_covers_every_tile():
     for (M, N, K, form) in [(4096, 4096, 4096, PAIR), (8192, 8192, 8192, PAIR), (8191, 1000, 777, SINGLE),
                             (16384, 64, 4096, SINGLE), (1000, 1300, 2056, PAIR)]:
         p = plan(M, N, K, form)
-        tiles_m, tiles_n = -(-M // 128), -(-N // 256)
+        tiles_m, tiles_n = -(-M // 128), -(-N // p["bn"])
         units = tiles_n * (-(-tiles_m // 2) if p["form"] != SINGLE else tiles_m)
         assert p["dp_units"] + p["split_units"] == units, (M, N, K, form)
         assert p["ctas"] == p["units"] * (1 if p["form"] == SINGLE else 2)
@@ -75,3 +76,19 @@ def test_argument_errors():
         assert binding.sgemm_3xtf32_plan(4, 4, 4, form, PAIRS, SMS)[0] == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_3xtf32_plan(4, 4, 4, PAIR, -1, SMS)[0] == binding.SGEMM_ERR_INVALID_VALUE
     assert binding.sgemm_3xtf32_plan(4, 4, 4, PAIR, PAIRS, 0)[0] == binding.SGEMM_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("form", [PAIR, SINGLE])
+@pytest.mark.parametrize("N", [1, 33, 64])
+def test_narrow_tiles_for_n_up_to_64(N, form):
+    # 16384 x N x 4096: 128 tiles of 128 x 64 (not 128 x 256) on single CTAs,
+    # 32-wide slices at any K: 48 KB stages, four of them
+    for K in (777, 4096):
+        p = plan(16384, N, K, form)
+        assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 64, 32, 4), K
+        assert p["dp_units"] + p["split_units"] == 128
+
+
+def test_wide_tiles_from_n_65():
+    for N in (65, 96, 256, 4096):
+        assert plan(4096, N, 4096, SINGLE)["bn"] == 256, N
