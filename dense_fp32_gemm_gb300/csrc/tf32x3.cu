@@ -683,10 +683,22 @@ struct Plan {
 Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   Plan pl{};
   pl.form = (want != kSingle && pairs > 0) ? want : (int)kSingle;
-  // N <= 64: 64-wide tiles (single CTAs), so that the MMAs compute no
+  // 64-wide tiles (single CTAs) for N <= 64, so that the MMAs compute no
   // columns beyond N -- a 256-wide tile would spend three quarters of its
-  // tensor-core work on them (16384 x 64 x 4096: 89.7 us against 149)
-  pl.bn = N <= BN_NARROW ? BN_NARROW : BN;
+  // tensor-core work on them (16384 x 64 x 4096: 89.7 us against 149) --
+  // and for problems with little 256-wide work: at most 48 wide tiles and
+  // tiles x K at most 32 x 2048, where most SMs would get a slice of a split
+  // tile each. Measured on GB300 (us, 64-wide against 256-wide): 512^3 22.5 /
+  // 45.1, 1024^3 34.9 / 44.5, 512 x 512 x 8192 58.5 / 92.6, 1024 x 1024 x 2048
+  // 53.6 / 53.9; past either bound the wide tile wins: 1024 x 1024 x 4096
+  // 90.0 / 68.1, 2048 x 1024 x 1024 (64 tiles) 49.2 / 45.1, 1024 x 1024 x
+  // 16384 314 / 179.
+  constexpr long long kNarrowMaxWideTiles = 48, kNarrowMaxTileK = 32LL * 2048;
+  const long long wide_tiles = (long long)ceil_div_nn(M, BM) * ceil_div_nn(N, BN);
+  pl.bn = (N <= BN_NARROW ||
+           (wide_tiles <= kNarrowMaxWideTiles && wide_tiles * K <= kNarrowMaxTileK))
+              ? BN_NARROW
+              : BN;
   if (pl.bn != BN) pl.form = kSingle;
   // schedule: whole tiles, then the last one to two waves split along K. In
   // the pair form a schedule unit is two vertically adjacent tiles (a tile

@@ -99,11 +99,18 @@ def test_sweep_integer_bit_exact(n):
 
 
 def test_slice_width_follows_k(kernel_form):
-    # single CTAs: BK = 32 (two stages) below K = 1024, BK = 16 (four stages) from there
-    H.check_against_oracle(Workload("x3k", 200, 300, 1023, 1.0, 0.5, "int3", 38), fn=X3)
+    # single CTAs with 256-wide tiles (here 17 x 11 of them): BK = 32 (two
+    # stages) below K = 1024, BK = 16 (four stages) from there
+    H.check_sampled(Workload("x3k", 2100, 2600, 1023, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
+                    fn=X3)
     assert "128x256x32_s2" in binding.sgemm_last_config()
-    H.check_against_oracle(Workload("x3k", 200, 300, 1024, 1.0, 0.5, "int3", 38), fn=X3)
+    H.check_sampled(Workload("x3k", 2100, 2600, 1024, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
+                    fn=X3)
     assert "128x256x16_s4" in binding.sgemm_last_config()
+    # at most 48 wide tiles: 64-wide tiles, BK = 32 at any K
+    for K in (1023, 1024):
+        H.check_against_oracle(Workload("x3k", 200, 300, K, 1.0, 0.5, "int3", 38), fn=X3)
+        assert "128x64x32_s4" in binding.sgemm_last_config()
     # whole waves of tile pairs at K = 1024: the two-SM form keeps BK = 32
     # (three stages of half B tiles), single CTAs take BK = 16
     H.check_sampled(Workload("x3k2", 128 * 2 * 76 * 2, 256, 1024, 1.0, 0.5, "int3", 39),

@@ -45,8 +45,8 @@ def test_pairs_fall_back_without_resident_pairs():
 
 @pytest.mark.parametrize("K, bk, stages", [(1023, 32, 2), (1024, 16, 4), (777, 32, 2), (16384, 16, 4)])
 def test_single_cta_slice_width_follows_k(K, bk, stages):
-    p = plan(300, 520, K, SINGLE)
-    assert (p["bk"], p["stages"], p["kiters"]) == (bk, stages, (K + bk - 1) // bk)
+    p = plan(2100, 2600, K, SINGLE)      # 17 x 11 wide tiles
+    assert (p["bn"], p["bk"], p["stages"], p["kiters"]) == (256, bk, stages, (K + bk - 1) // bk)
 
 
 def test_two_sm_form_keeps_32_wide_slices_at_any_k():
@@ -89,6 +89,24 @@ def test_narrow_tiles_for_n_up_to_64(N, form):
         assert p["dp_units"] + p["split_units"] == 128
 
 
-def test_wide_tiles_from_n_65():
+def test_wide_tiles_from_n_65_with_more_than_48_of_them():
     for N in (65, 96, 256, 4096):
-        assert plan(4096, N, 4096, SINGLE)["bn"] == 256, N
+        assert plan(16384, N, 4096, SINGLE)["bn"] == 256, N   # at least 128 wide tiles
+    assert plan(2048, 2048, 2048, SINGLE)["bn"] == 256      # 128 wide tiles
+    assert plan(6272, 256, 512, SINGLE)["bn"] == 256        # 49 wide tiles
+
+
+@pytest.mark.parametrize("M, N, K", [(512, 512, 512), (1024, 1024, 1024), (1536, 768, 1024),
+                                     (6144, 256, 512), (300, 520, 4096), (512, 512, 8192),
+                                     (1024, 1024, 2048)])
+def test_narrow_tiles_for_little_wide_work(M, N, K):
+    # at most 48 wide tiles and wide tiles x K at most 32 x 2048
+    p = plan(M, N, K, PAIR)
+    assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 64, 32, 4)
+
+
+@pytest.mark.parametrize("M, N, K", [(1024, 1024, 4096), (1024, 1024, 16384), (512, 2048, 4096),
+                                     (1536, 1024, 3072), (2048, 1024, 1024), (1024, 1024, 3072)])
+def test_wide_tiles_past_either_bound(M, N, K):
+    assert plan(M, N, K, SINGLE)["bn"] == 256
+
