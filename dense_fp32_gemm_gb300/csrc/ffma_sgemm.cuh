@@ -359,15 +359,14 @@ __global__ void __launch_bounds__(kernel_threads<Cfg, AL>(), Cfg::S.MINB)
                                            kDevTimeoutFull, p.timeout_ns));
         if (!ok) break;
         transpose_slot(Stg + j * (BM * BK), As + slot * A_ST);
-        // the warp's stores are ordered before lane 0's release on fullA; and
-        // every lane's loads from staging slot j are complete (their values
-        // were stored above), so the slot may be refilled by the async proxy
+        // each lane orders its reads of staging slot j before the async-proxy
+        // write that refills it; the warp sync then orders every lane's
+        // stores and reads before lane 0's release on fullA and its TMA
+        const bool refill = a_issued < nsteps;
+        if (refill) ptx::fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bb->fullA[slot]));
-        if (a_issued < nsteps) {
-          ptx::fence_proxy_async_shared();
-          issue_staging();
-        }
+        if (refill) issue_staging();
         cur_next(cb);
       }
       if (!ok && lane == 0) {
