@@ -99,12 +99,13 @@ def test_sweep_integer_bit_exact(n):
 
 
 def test_slice_width_follows_k(kernel_form):
-    # single CTAs with 256-wide tiles (here 17 x 11 of them): BK = 32 (two
+    # single CTAs with 256-wide tiles (17 x 6 of them: 54 tile pairs, fewer
+    # than the 76 clusters, so the pair form falls back): BK = 32 (two
     # stages) below K = 1024, BK = 16 (four stages) from there
-    H.check_sampled(Workload("x3k", 2100, 2600, 1023, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
+    H.check_sampled(Workload("x3k", 2100, 1300, 1023, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
                     fn=X3)
     assert "128x256x32_s2" in binding.sgemm_last_config()
-    H.check_sampled(Workload("x3k", 2100, 2600, 1024, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
+    H.check_sampled(Workload("x3k", 2100, 1300, 1024, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
                     fn=X3)
     assert "128x256x16_s4" in binding.sgemm_last_config()
     # at most 48 wide tiles: 64-wide tiles, BK = 32 at any K

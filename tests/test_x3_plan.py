@@ -21,10 +21,11 @@ def plan(M, N, K, form, pairs=PAIRS, sms=SMS):
 
 
 def test_square4096_in_each_form():
-    # 32 x 16 tiles of 128 x 256: 256 tile pairs on 76 clusters
+    # 32 x 16 tiles of 128 x 256: 256 tile pairs on 76 clusters, 3.37 waves:
+    # three waves whole, the last (a 0.37 wave, at least a quarter) split along K
     p = plan(4096, 4096, 4096, PAIR)
     assert (p["form"], p["bk"], p["stages"], p["ctas"], p["units"], p["bn"]) == (PAIR, 32, 3, 152, 76, 256)
-    assert (p["dp_units"], p["split_units"], p["kiters"]) == (152, 104, 128)
+    assert (p["dp_units"], p["split_units"], p["kiters"]) == (228, 28, 128)
     p = plan(4096, 4096, 4096, SINGLE)
     assert (p["form"], p["bk"], p["stages"], p["ctas"], p["units"]) == (SINGLE, 16, 4, 152, 152)
     assert (p["dp_units"], p["split_units"]) == (304, 208)
@@ -110,3 +111,13 @@ def test_narrow_tiles_for_little_wide_work(M, N, K):
 def test_wide_tiles_past_either_bound(M, N, K):
     assert plan(M, N, K, SINGLE)["bn"] == 256
 
+
+
+def test_pair_form_splits_the_last_two_waves_when_the_last_is_thin():
+    # 6144 x 4096: 384 tile pairs, 5.05 waves on 76 clusters: the last 0.05 of a
+    # wave is too thin to split alone, so the last two waves are split
+    p = plan(6144, 4096, 4096, PAIR)
+    assert p["form"] == PAIR and p["dp_units"] == 4 * 76 and p["split_units"] == 384 - 4 * 76
+    # 8192^3: 1024 pairs, 13.47 waves: only the last wave is split
+    p = plan(8192, 8192, 8192, PAIR)
+    assert p["dp_units"] == 13 * 76 and p["split_units"] == 1024 - 13 * 76
