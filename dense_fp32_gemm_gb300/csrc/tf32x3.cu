@@ -718,13 +718,16 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   if (pl.form != kSingle) {
     // groups of 8 tile-row pairs in the raster (measured at 8192^3: 309 against
     // 305 TFLOP/s with 4, 298 with 2; 16 the same as 8)
-    // whole pair tiles, then a K split of the last wave when it is at least a
-    // quarter full, else of the last two (measured at 4096^3, 3.37 waves:
+    // whole pair tiles, then, with at least two waves of them, a K split of
+    // the last wave when it is at least a quarter full, else of the last two
+    // (below two waves the two-wave split leaves no whole tiles, and single
+    // CTAs run: 3072 x 2048 x 1536 190 TFLOP/s against 174 for pairs with
+    // only the last wave split). Measured at 4096^3, 3.37 waves:
     // 284.8 against 273.3 TFLOP/s; 5120^3: 305.3 against 297.9; 8192^3, 13.5
     // waves: 323.3 against 319.7; 6144 x 4096 x 4096, 5.05 waves: splitting
     // only the last 0.05 of a wave lost 8 %)
     const long long units = (long long)((tiles_m + 1) / 2) * tiles_n;
-    const bool full_tail = pairs > 0 && units > pairs && (units % pairs) * 4 >= pairs;
+    const bool full_tail = pairs > 0 && units >= 2LL * pairs && (units % pairs) * 4 >= pairs;
     pl.sched = make_schedule((tiles_m + 1) / 2, tiles_n, pl.kiters, pairs,
                              SchedPolicy{full_tail ? kSchedHybridTail : kSchedHybrid, 8,
                                          64 / pl.bk, 1});
