@@ -121,3 +121,11 @@ def test_pair_form_splits_the_last_two_waves_when_the_last_is_thin():
     # 8192^3: 1024 pairs, 13.47 waves: only the last wave is split
     p = plan(8192, 8192, 8192, PAIR)
     assert p["dp_units"] == 13 * 76 and p["split_units"] == 1024 - 13 * 76
+
+
+def test_below_two_waves_of_pairs_single_ctas_run():
+    # 3072 x 2048: 96 tile pairs, 1.26 waves on 76 clusters: the two-wave split
+    # leaves no whole tiles, so single CTAs run (faster than pairs with a
+    # one-wave split)
+    p = plan(3072, 2048, 1536, PAIR)
+    assert (p["form"], p["dp_units"]) == (SINGLE, 0)
