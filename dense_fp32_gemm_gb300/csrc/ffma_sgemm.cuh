@@ -247,6 +247,15 @@ __global__ void __launch_bounds__(kernel_threads<Cfg, AL>(), Cfg::S.MINB)
     if (BL == kBRowTma) ptx::tma_prefetch_desc(&tmapB);
   }
   __syncthreads();
+  // Launched with programmatic stream serialization, this grid may start
+  // while the kernel before it on the stream is finishing: the set-up above
+  // touches only shared memory and the parameters, and nothing below reads or
+  // writes global memory before that kernel has completed. The next grid may
+  // launch now (its own wait protects this grid's results).
+#if SGEMM_GB300_PDL
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+#endif
 
   const int npieces = num_pieces(sc, b);
   const int nsteps = (int)total_steps(sc, b);

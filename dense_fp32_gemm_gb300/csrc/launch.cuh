@@ -66,12 +66,29 @@ struct Launcher {
     }
   }
 
+  // Launched with programmatic stream serialization: the grid may start while
+  // the kernel before it on the stream finishes (the kernel waits for it
+  // before any global memory access).
   template <int AL, int BL>
   static cudaError_t go(int grid, const KernelParams& p, const CUtensorMap* ma,
                         const CUtensorMap* mb, cudaStream_t stream) {
+#if SGEMM_GB300_PDL
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.gridDim = dim3((unsigned)grid);
+    lc.blockDim = dim3((unsigned)kernel_threads<Cfg, AL>());
+    lc.dynamicSmemBytes = (size_t)smem_of<AL>();
+    lc.stream = stream;
+    lc.attrs = la;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, ffma_sgemm_kernel<Cfg, AL, BL>, p, *ma, *mb);
+#else
     ffma_sgemm_kernel<Cfg, AL, BL>
         <<<grid, kernel_threads<Cfg, AL>(), smem_of<AL>(), stream>>>(p, *ma, *mb);
     return cudaGetLastError();
+#endif
   }
 
   static cudaError_t launch(int al, int bl, int grid, const KernelParams& p,

@@ -145,6 +145,15 @@ __device__ __forceinline__ uint32_t ld_shared_cluster(uint32_t cluster_addr) {
   return v;
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory operations are visible (returns at once
+// when the grid was launched without such a dependency) ...
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and allow the grid launched after this one to start.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Hint: bring the 128-byte line holding `p` into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

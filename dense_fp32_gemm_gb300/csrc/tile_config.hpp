@@ -19,6 +19,10 @@
 namespace sgemm_gb300 {
 
 constexpr int kWarp = 32;
+// FFMA launches use programmatic dependent launch (launch.cuh, ffma_sgemm.cuh).
+#ifndef SGEMM_GB300_PDL
+#define SGEMM_GB300_PDL 1
+#endif
 // Shared memory a CTA may use on sm_103a (opt-in maximum per block).
 constexpr int kMaxSmemPerCta = 227 * 1024;
 // Padding (in floats) added to each k-row of the transposed A tile. With the
