@@ -310,6 +310,10 @@ __global__ void __launch_bounds__(NT, 1)
     }
   }
   if (TWO_SM) __syncthreads();  // every role sees the abort word
+  // Launched with programmatic stream serialization after the B^T pre-pass:
+  // the set-up above (barriers, TMEM, the cluster rendezvous) overlaps its
+  // end; nothing below touches global memory before it has completed.
+  ptx::griddep_wait();
 
   if (warp == 0) {
     // ---- TMA producer: the raw A and B^T tiles of every k-slice of every piece
@@ -917,34 +921,35 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   p.epoch = epoch;
   p.status = status;
   p.timeout_ns = library_wait_timeout_ns();
-  if (CL == 1) {
-    using x3::BN_NARROW;
-    if (bn == BN_NARROW && bk == 16)
-      x3::gemm_kernel<x3::kSingle, 16, BN_NARROW>
-          <<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
-    else if (bn == BN_NARROW)
-      x3::gemm_kernel<x3::kSingle, 32, BN_NARROW>
-          <<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
-    else if (bk == 16)
-      x3::gemm_kernel<x3::kSingle, 16><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
-    else
-      x3::gemm_kernel<x3::kSingle, 32><<<ctas, x3::NT, x3::SMEM_BYTES, stream>>>(p, mA, mB);
-    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-  } else {
+  {
+    // programmatic stream serialization (the kernel waits for the pre-pass
+    // before any global access), and clusters of two for the pair form
     cudaLaunchConfig_t lc = {};
-    cudaLaunchAttribute la[1];
-    la[0].id = cudaLaunchAttributeClusterDimension;
-    la[0].val.clusterDim.x = 2;
-    la[0].val.clusterDim.y = 1;
-    la[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute la[2];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    la[1].id = cudaLaunchAttributeClusterDimension;
+    la[1].val.clusterDim.x = 2;
+    la[1].val.clusterDim.y = 1;
+    la[1].val.clusterDim.z = 1;
     lc.gridDim = dim3((unsigned)ctas);
     lc.blockDim = dim3(x3::NT);
     lc.dynamicSmemBytes = x3::SMEM_BYTES;
     lc.stream = stream;
     lc.attrs = la;
-    lc.numAttrs = 1;
-    // the two-SM form always runs 32-wide slices (make_plan)
-    const cudaError_t e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kTwoSmPair, 32>, p, mA, mB);
+    lc.numAttrs = CL == 2 ? 2 : 1;
+    using x3::BN_NARROW;
+    cudaError_t e;
+    if (CL == 2)  // the two-SM form always runs 32-wide slices (make_plan)
+      e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kTwoSmPair, 32>, p, mA, mB);
+    else if (bn == BN_NARROW && bk == 16)
+      e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 16, BN_NARROW>, p, mA, mB);
+    else if (bn == BN_NARROW)
+      e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 32, BN_NARROW>, p, mA, mB);
+    else if (bk == 16)
+      e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 16>, p, mA, mB);
+    else
+      e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 32>, p, mA, mB);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return SGEMM_ERR_LAUNCH;
