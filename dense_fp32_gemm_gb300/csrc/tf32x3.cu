@@ -195,6 +195,9 @@ __global__ void pack_a_kernel(int M, int K, const float* __restrict__ A, long lo
 __global__ void transpose_b_kernel(int K, int N, const float* __restrict__ B, long long ldb,
                                    float* __restrict__ bt, long long ldw, int k_base) {
   __shared__ float tile[32][33];
+  // may be launched before the kernel ahead of it on the stream has finished
+  // (programmatic dependent launch): wait for it before touching memory
+  ptx::griddep_wait();
   const int n0 = blockIdx.x * 32, k0 = k_base + blockIdx.y * 32;
   const int kn = K - k0, nn = N - n0;             // both > 0
   const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
@@ -312,8 +315,10 @@ __global__ void __launch_bounds__(NT, 1)
   if (TWO_SM) __syncthreads();  // every role sees the abort word
   // Launched with programmatic stream serialization after the B^T pre-pass:
   // the set-up above (barriers, TMEM, the cluster rendezvous) overlaps its
-  // end; nothing below touches global memory before it has completed.
+  // end; nothing below touches global memory before it has completed. The
+  // next call's pre-pass may then launch (it waits for this grid in turn).
   ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     // ---- TMA producer: the raw A and B^T tiles of every k-slice of every piece
@@ -890,8 +895,22 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     constexpr long long kRowsPerGrid = 65535LL * 32;  // tile rows of one grid (gridDim.y)
     for (long long kb = 0; kb < K; kb += kRowsPerGrid) {
       const int ktiles = ceil_div_nn((int)(K - kb < kRowsPerGrid ? K - kb : kRowsPerGrid), 32);
-      dim3 grid((unsigned)ceil_div_nn(N, 32), (unsigned)ktiles), block(32, 8);
-      x3::transpose_b_kernel<<<grid, block, 0, stream>>>(K, N, B, ldb, bt, Kp, (int)kb);
+      // programmatic dependent launch: the grid waits for the kernel ahead of
+      // it (the previous call's GEMM reads this workspace) before any access
+      cudaLaunchConfig_t tc = {};
+      cudaLaunchAttribute ta[1];
+      ta[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      ta[0].val.programmaticStreamSerializationAllowed = 1;
+      tc.gridDim = dim3((unsigned)ceil_div_nn(N, 32), (unsigned)ktiles);
+      tc.blockDim = dim3(32, 8);
+      tc.stream = stream;
+      tc.attrs = ta;
+      tc.numAttrs = 1;
+      if (cudaLaunchKernelEx(&tc, x3::transpose_b_kernel, K, N, B, (long long)ldb, bt, Kp,
+                             (int)kb) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+      }
     }
     if (!a_direct) {
       const int bx = (K + 255) / 256 < 8 ? (K + 255) / 256 : 8;
