@@ -39,6 +39,11 @@ __global__ void __launch_bounds__(kThreads) tiny_kernel(int M, int N, int K, flo
   const int t = threadIdx.x;
   const int tr = (t / 16) * 2, tc = (t % 16) * 2;  // this thread's 2 x 2 outputs
   float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+  // launched with programmatic dependent launch: wait for the kernel ahead of
+  // this one on the stream before touching global memory, then let the next
+  // one launch (it waits for this grid in turn)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   for (int k0 = 0; k0 < K; k0 += kKC) {
     const int kc = (K - k0) < kKC ? (K - k0) : kKC;
@@ -135,15 +140,26 @@ cudaError_t tiny_launch(int dev, int M, int N, int K, float alpha, const float* 
   const int grid = tiles_m * tiles_n;  // at most 2^25 / 32 tiles
   const bool vec = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) == 0 &&
                    (lda % 4) == 0 && (ldb % 4) == 0;
-  if (vec)
-    tiny_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(M, N, K, alpha, A, lda, B, ldb, beta,
-                                                              C, ldc, tiles_n);
-  else
-    tiny_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(M, N, K, alpha, A, lda, B, ldb,
-                                                               beta, C, ldc, tiles_n);
+  // programmatic dependent launch: the launch overlaps the end of the kernel
+  // ahead (the kernel waits for it before any global access)
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.gridDim = dim3((unsigned)grid);
+  lc.blockDim = dim3(kThreads);
+  lc.dynamicSmemBytes = kSmemBytes;
+  lc.stream = stream;
+  lc.attrs = la;
+  lc.numAttrs = 1;
+  const cudaError_t e =
+      vec ? cudaLaunchKernelEx(&lc, tiny_kernel<true>, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                               ldc, tiles_n)
+          : cudaLaunchKernelEx(&lc, tiny_kernel<false>, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                               ldc, tiles_n);
   snprintf(text, (size_t)text_len, "tiny_32x32_k%d %s grid=%d", kKC, vec ? "vec128" : "scalar",
            grid);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace sgemm_gb300
