@@ -180,9 +180,13 @@ int ctx_for(int dev, cudaStream_t user, HostCtx** out) {
   return SGEMM_OK;
 }
 
-// C = C + beta * C0 (both M x N, dense).
+// C = C + beta * C0 (both M x N, dense). Launched with programmatic
+// dependent launch after the panel's GEMM: it waits for that GEMM before
+// touching memory, and lets the next panel's GEMM launch.
 __global__ void add_scaled_kernel(long long n, float beta, float* __restrict__ C,
                                   const float* __restrict__ C0) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n;
        e += (long long)gridDim.x * blockDim.x)
     C[e] = fmaf(beta, C0[e], C[e]);
@@ -336,7 +340,18 @@ SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float* A, int l
         if (cudaStreamWaitEvent(user, c->c_in_panel[pi], 0) != cudaSuccess) return fail();
         int pb = (int)((pn + 255) / 256);
         if (pb > sms * 8) pb = sms * 8;
-        add_scaled_kernel<<<pb, 256, 0, user>>>((long long)pn, beta, dCp, c->dC0 + (size_t)r0 * N);
+        cudaLaunchConfig_t lc = {};
+        cudaLaunchAttribute la[1];
+        la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        la[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.gridDim = dim3((unsigned)pb);
+        lc.blockDim = dim3(256);
+        lc.stream = user;
+        lc.attrs = la;
+        lc.numAttrs = 1;
+        if (cudaLaunchKernelEx(&lc, add_scaled_kernel, (long long)pn, beta, dCp,
+                               (const float*)(c->dC0 + (size_t)r0 * N)) != cudaSuccess)
+          return fail();
       }
       if (cudaEventRecord(c->panel[pi], user) != cudaSuccess ||
           cudaStreamWaitEvent(c->d2h, c->panel[pi], 0) != cudaSuccess ||
