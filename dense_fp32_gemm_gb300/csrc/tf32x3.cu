@@ -41,6 +41,10 @@
 //     remote arrival per stage); its commits free the stage and publish the
 //     accumulator in both CTAs; its MMA thread waits for both epilogues.
 //   * single CTAs, each with its own A and B tiles.
+//   * 64-wide tiles (N <= 64, or little 256-wide work): single CTAs whose
+//     converter warps store A's raw values and residuals into tensor memory
+//     (tcgen05.st), where the MMAs read A; shared memory holds A's raw tile
+//     and B's two parts, so a stage is 32 KB and six fit.
 // Each CTA loads only its own tiles; no TMA load is multicast.
 // Before exiting, a CTA of a pair waits (bounded) until its barriers have
 // received the peer's last arrivals, then meets the peer at a cluster
@@ -91,9 +95,10 @@ constexpr int kMaxStages = 6;
 // tile, and BK = 32 gives three 64 KB stages (its hand-offs between the CTAs
 // of a pair cost more, so it always takes 32; 16-wide stages measured 158
 // against 265 TFLOP/s at 4096^3).
-// BNT: the tile's width in N (BN, or 64 for N <= 64: see make_plan); a
-// narrow tile keeps the configured stage count, up to kMaxStages.
-template <int BK_, int B_PARTS = 1, int BNT = BN>
+// BNT: the tile's width in N (BN, or 64: see make_plan); a narrow tile gets
+// as many stages as fit, up to kMaxStages. A_TMEM (the 64-wide tile): A's
+// parts live in tensor memory, so a stage holds only A's raw tile for them.
+template <int BK_, int B_PARTS = 1, int BNT = BN, bool A_TMEM = false>
 struct Slice {
   static constexpr int BK = BK_;
   static_assert(BK == 32 || BK == 16, "k-slice width");
@@ -101,8 +106,10 @@ struct Slice {
   static constexpr int A_BYTES = BM * BK * 4;                      // one of A_hi, A_lo
   static constexpr int B_BYTES = BNT / B_PARTS * BK * 4;           // one of B_hi, B_lo
   // a stage: [A_hi | A_lo | B_hi | B_lo]; TMA writes the _hi tiles (the raw
-  // values), the converter warps the _lo tiles
-  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;   // 96 / 48 KB, or 64 / 32 KB
+  // values), the converter warps the _lo tiles. A_TMEM: [A_hi | B_hi | B_lo],
+  // the converters put A's two parts in tensor memory instead
+  static constexpr int B_OFF = (A_TMEM ? 1 : 2) * A_BYTES;        // B_hi in a stage
+  static constexpr int STAGE_BYTES = B_OFF + 2 * B_BYTES;  // 96 / 48 KB, 64 KB pairs, 32 KB narrow
   static constexpr int ST = kStageRegion / STAGE_BYTES < kMaxStages
                                 ? kStageRegion / STAGE_BYTES
                                 : kMaxStages;                      // 2 / 4, or 3 / 6
@@ -114,7 +121,8 @@ static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
               "every width fills the same stage region");
 constexpr int NBUF = 2;                   // accumulators, so the epilogue overlaps the next MMAs
 // One FP32 accumulator is 128 lanes x BNT columns; NBUF of them (all 512
-// columns for BNT = BN, 128 for the 64-wide tile).
+// columns for BNT = BN, 128 for the 64-wide tile, whose A slots take the
+// other 384).
 constexpr int tmem_cols(int bnt) { return NBUF * bnt; }
 // Kernel forms (the values sgemm_3xtf32_set_kernel_form takes): single CTAs;
 // CTA pairs whose even CTA issues M = 256 MMAs over both (cta_group::2),
@@ -122,7 +130,8 @@ constexpr int tmem_cols(int bnt) { return NBUF * bnt; }
 enum Form : int { kSingle = 1, kTwoSmPair = 2 };
 // Stages of a (form, k-slice width, tile width): Slice<>::ST, for the host.
 constexpr int stages_of(int form, int bk, int bnt) {
-  const int stage = 2 * BM * bk * 4 + 2 * (bnt / (form == kTwoSmPair ? 2 : 1)) * bk * 4;
+  const bool a_tmem = form == kSingle && bnt != BN;  // the kernel's A_TM
+  const int stage = (a_tmem ? 1 : 2) * BM * bk * 4 + 2 * (bnt / (form == kTwoSmPair ? 2 : 1)) * bk * 4;
   return kStageRegion / stage < kMaxStages ? kStageRegion / stage : kMaxStages;
 }
 constexpr int EPI_THREADS = 128;          // warps 2-5
@@ -255,9 +264,19 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr int CL = TWO_SM ? 2 : 1;                // CTAs per cluster
   constexpr int CG = TWO_SM ? 2 : 1;                // cta_group of every tcgen05 instruction
   static_assert(BNT == BN || (!TWO_SM && BNT % 16 == 0 && BNT >= 32), "tile width");
-  using S = Slice<BK, TWO_SM ? 2 : 1, BNT>;
+  // 64-wide tiles keep A's two TF32 parts in tensor memory (the MMAs read A
+  // from there, B from shared memory): each stage then moves a third less
+  // through shared memory, whose bandwidth the narrow tile's stages are
+  // bound by
+  constexpr bool A_TM = !TWO_SM && BNT != BN;
+  static_assert(!A_TM || BK == 32, "A in tensor memory: 32-wide slices");
+  using S = Slice<BK, TWO_SM ? 2 : 1, BNT, A_TM>;
   constexpr int ACC_COLS = BNT;
-  constexpr int TMEM_COLS = tmem_cols(BNT);
+  constexpr int A_TCOL0 = NBUF * BNT;  // A slots after the accumulators: [hi | lo] per stage
+  constexpr int A_TCOLS = 2 * BK;
+  constexpr int TMEM_COLS = A_TM ? 512 : tmem_cols(BNT);
+  static_assert(!A_TM || A_TCOL0 + S::ST * A_TCOLS <= TMEM_COLS, "tensor memory columns");
+  constexpr int B_OFF = S::B_OFF;
   constexpr uint32_t IDESC = tc::idesc_tf32(BM, BNT);
   constexpr int ST = S::ST, ROW_BYTES = S::ROW_BYTES;
   constexpr int A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES, STAGE_BYTES = S::STAGE_BYTES;
@@ -344,9 +363,9 @@ __global__ void __launch_bounds__(NT, 1)
           ptx::tma_load_2d(st0, &tmA, kb * BK, tm * BM, fb);
           if (TWO_SM) {
             // this CTA's half of the B tile (N columns 128 * rank ..), into this CTA
-            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BN + rank * (BN / 2), fb);
+            ptx::tma_load_2d(st0 + B_OFF, &tmB, kb * BK, tn * BN + rank * (BN / 2), fb);
           } else {
-            ptx::tma_load_2d(st0 + 2 * A_BYTES, &tmB, kb * BK, tn * BNT, fb);
+            ptx::tma_load_2d(st0 + B_OFF, &tmB, kb * BK, tn * BNT, fb);
           }
         }
         if (!ok) break;
@@ -430,12 +449,19 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 8; ++kk) {
             const uint32_t koff = (uint32_t)(kk * 32);  // 8 TF32 values = 32 bytes
+            const uint64_t b_hi = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + B_OFF + koff);
+            const uint64_t b_lo = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + B_OFF + B_BYTES + koff);
+            const uint32_t first = (kb == pc.kb && kk == 0) ? 0u : 1u;
+            if (A_TM) {
+              // A's parts in the stage's tensor-memory slot: 8 columns per 8 values of K
+              const uint32_t a_hi = tmem + (uint32_t)(A_TCOL0 + s * A_TCOLS + kk * 8);
+              tc::mma_tf32_ts(d, a_hi, b_hi, IDESC, first);
+              tc::mma_tf32_ts(d, a_hi, b_lo, IDESC, 1u);
+              tc::mma_tf32_ts(d, a_hi + (uint32_t)BK, b_hi, IDESC, 1u);
+              continue;
+            }
             const uint64_t a_hi = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + koff);
             const uint64_t a_lo = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + A_BYTES + koff);
-            const uint64_t b_hi = tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + 2 * A_BYTES + koff);
-            const uint64_t b_lo =
-                tc::smem_desc_k_swizzled<ROW_BYTES>(st0 + 2 * A_BYTES + B_BYTES + koff);
-            const uint32_t first = (kb == pc.kb && kk == 0) ? 0u : 1u;
             if (TWO_SM) {
               tc::mma_tf32_pair(d, a_hi, b_hi, IDESC_PAIR, first);
               tc::mma_tf32_pair(d, a_hi, b_lo, IDESC_PAIR, 1u);
@@ -490,15 +516,48 @@ __global__ void __launch_bounds__(NT, 1)
         }
         unsigned char* st = base + s * STAGE_BYTES;
         const float4* a_raw = reinterpret_cast<const float4*>(st);
-        float4* a_lo = reinterpret_cast<float4*>(st + A_BYTES);
-        const float4* b_raw = reinterpret_cast<const float4*>(st + 2 * A_BYTES);
-        float4* b_lo = reinterpret_cast<float4*>(st + 2 * A_BYTES + B_BYTES);
+        const float4* b_raw = reinterpret_cast<const float4*>(st + B_OFF);
+        float4* b_lo = reinterpret_cast<float4*>(st + B_OFF + B_BYTES);
+        if (A_TM) {
+          // this thread's row of the A tile (the warp may reach TMEM lanes
+          // 32 * (warp % 4) ..): its 32 raw values into the stage's hi
+          // columns, their residuals into the lo columns. The 16-byte chunks
+          // of a row sit at the 128-byte swizzle's positions.
+          const int r = (warp & 3) * 32 + lane;
+          uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int q = ct; q < A_BYTES / 16; q += CONV_THREADS) a_lo[q] = tf32_residual4(a_raw[q]);
+          for (int c = 0; c < 8; ++c) {
+            const float4 v = a_raw[r * 8 + (c ^ (r & 7))];
+            const float4 l = tf32_residual4(v);
+            hi[4 * c] = __float_as_uint(v.x);
+            hi[4 * c + 1] = __float_as_uint(v.y);
+            hi[4 * c + 2] = __float_as_uint(v.z);
+            hi[4 * c + 3] = __float_as_uint(v.w);
+            lo[4 * c] = __float_as_uint(l.x);
+            lo[4 * c + 1] = __float_as_uint(l.y);
+            lo[4 * c + 2] = __float_as_uint(l.z);
+            lo[4 * c + 3] = __float_as_uint(l.w);
+          }
+          // the MMAs that read this slot last have completed (they freed the
+          // stage before its raw tiles were loaded again)
+          tc::fence_after_sync();
+          const uint32_t slot_t =
+              tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(A_TCOL0 + s * A_TCOLS);
+          tc::tmem_st32(slot_t, hi);
+          tc::tmem_st32(slot_t + (uint32_t)BK, lo);
+        } else {
+          float4* a_lo = reinterpret_cast<float4*>(st + A_BYTES);
+#pragma unroll
+          for (int q = ct; q < A_BYTES / 16; q += CONV_THREADS) a_lo[q] = tf32_residual4(a_raw[q]);
+        }
 #pragma unroll
         for (int q = ct; q < B_BYTES / 16; q += CONV_THREADS) b_lo[q] = tf32_residual4(b_raw[q]);
         // the MMAs read these tiles through the async proxy
         ptx::fence_proxy_async_shared();
+        if (A_TM) {
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+        }
         __syncwarp();
         if (lane == 0) {
           ptx::mbar_arrive(ptx::smem_addr(&bar->conv[s]));
@@ -827,8 +886,6 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
       using namespace x3;
       if (cudaFuncSetAttribute(gemm_kernel<kSingle, 16>, attr, SMEM_BYTES) != cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kSingle, 32>, attr, SMEM_BYTES) != cudaSuccess ||
-          cudaFuncSetAttribute(gemm_kernel<kSingle, 16, BN_NARROW>, attr, SMEM_BYTES) !=
-              cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kSingle, 32, BN_NARROW>, attr, SMEM_BYTES) !=
               cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kTwoSmPair, 32>, attr, SMEM_BYTES) != cudaSuccess) {
@@ -961,9 +1018,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     cudaError_t e;
     if (CL == 2)  // the two-SM form always runs 32-wide slices (make_plan)
       e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kTwoSmPair, 32>, p, mA, mB);
-    else if (bn == BN_NARROW && bk == 16)
-      e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 16, BN_NARROW>, p, mA, mB);
-    else if (bn == BN_NARROW)
+    else if (bn == BN_NARROW)  // 64-wide tiles always run 32-wide slices (make_plan)
       e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 32, BN_NARROW>, p, mA, mB);
     else if (bk == 16)
       e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 16>, p, mA, mB);

@@ -83,10 +83,11 @@ def test_argument_errors():
 @pytest.mark.parametrize("N", [1, 33, 64])
 def test_narrow_tiles_for_n_up_to_64(N, form):
     # 16384 x N x 4096: 128 tiles of 128 x 64 (not 128 x 256) on single CTAs,
-    # 32-wide slices at any K: 48 KB stages, four of them
+    # 32-wide slices at any K; A's two parts in tensor memory, so a stage
+    # holds A's raw tile and B's two parts (32 KB), six of them
     for K in (777, 4096):
         p = plan(16384, N, K, form)
-        assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 64, 32, 4), K
+        assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 64, 32, 6), K
         assert p["dp_units"] + p["split_units"] == 128
 
 
@@ -103,7 +104,7 @@ def test_wide_tiles_from_n_65_with_more_than_48_of_them():
 def test_narrow_tiles_for_little_wide_work(M, N, K):
     # at most 48 wide tiles and wide tiles x K at most 32 x 2048
     p = plan(M, N, K, PAIR)
-    assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 64, 32, 4)
+    assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 64, 32, 6)
 
 
 @pytest.mark.parametrize("M, N, K", [(1024, 1024, 4096), (1024, 1024, 16384), (512, 2048, 4096),
