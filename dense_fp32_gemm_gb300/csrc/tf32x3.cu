@@ -41,10 +41,11 @@
 //     remote arrival per stage); its commits free the stage and publish the
 //     accumulator in both CTAs; its MMA thread waits for both epilogues.
 //   * single CTAs, each with its own A and B tiles.
-//   * 64-wide tiles (N <= 64, or little 256-wide work): single CTAs whose
-//     converter warps store A's raw values and residuals into tensor memory
-//     (tcgen05.st), where the MMAs read A; shared memory holds A's raw tile
-//     and B's two parts, so a stage is 32 KB and six fit.
+//   * narrow tiles, 64 wide (N <= 64, or few tiles) or 128 wide (N <= 128,
+//     or little 256-wide work): single CTAs whose converter warps store A's raw values
+//     and residuals into tensor memory (tcgen05.st), where the MMAs read A;
+//     shared memory holds A's raw tile and B's two parts, so a stage is 32 KB
+//     (six fit) or 48 KB (four).
 // Each CTA loads only its own tiles; no TMA load is multicast.
 // Before exiting, a CTA of a pair waits (bounded) until its barriers have
 // received the peer's last arrivals, then meets the peer at a cluster
@@ -95,9 +96,10 @@ constexpr int kMaxStages = 6;
 // tile, and BK = 32 gives three 64 KB stages (its hand-offs between the CTAs
 // of a pair cost more, so it always takes 32; 16-wide stages measured 158
 // against 265 TFLOP/s at 4096^3).
-// BNT: the tile's width in N (BN, or 64: see make_plan); a narrow tile gets
-// as many stages as fit, up to kMaxStages. A_TMEM (the 64-wide tile): A's
-// parts live in tensor memory, so a stage holds only A's raw tile for them.
+// BNT: the tile's width in N (BN, or 64 or 128: see make_plan); a narrow
+// tile gets as many stages as fit, up to kMaxStages. A_TMEM (the narrow
+// tiles): A's parts live in tensor memory, so a stage holds only A's raw
+// tile for them.
 template <int BK_, int B_PARTS = 1, int BNT = BN, bool A_TMEM = false>
 struct Slice {
   static constexpr int BK = BK_;
@@ -121,8 +123,8 @@ static_assert(Slice<16>::ST * Slice<16>::STAGE_BYTES == kStageRegion &&
               "every width fills the same stage region");
 constexpr int NBUF = 2;                   // accumulators, so the epilogue overlaps the next MMAs
 // One FP32 accumulator is 128 lanes x BNT columns; NBUF of them (all 512
-// columns for BNT = BN, 128 for the 64-wide tile, whose A slots take the
-// other 384).
+// columns for BNT = BN; 128 or 256 for the narrow tiles, whose A slots take
+// the rest).
 constexpr int tmem_cols(int bnt) { return NBUF * bnt; }
 // Kernel forms (the values sgemm_3xtf32_set_kernel_form takes): single CTAs;
 // CTA pairs whose even CTA issues M = 256 MMAs over both (cta_group::2),
@@ -139,8 +141,9 @@ constexpr int CONV_WARP0 = 6;             // warps 6-9 write the residual tiles
 constexpr int CONV_THREADS = 128;
 constexpr uint32_t IDESC_PAIR = tc::idesc_tf32(2 * BM, BN);  // M = 256 over a CTA pair
 static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
-// the narrow tile of problems with N <= 64
-constexpr int BN_NARROW = 64;
+// the narrow tiles: 64 wide for N <= 64 and problems of few tiles, 128 wide
+// for N <= 128 and problems with little 256-wide work (make_plan)
+constexpr int BN_NARROW = 64, BN_MID = 128;
 
 struct Barriers {
   uint64_t full[kMaxStages];   // TMA transaction bytes of one stage (the raw tiles)
@@ -264,10 +267,9 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr int CL = TWO_SM ? 2 : 1;                // CTAs per cluster
   constexpr int CG = TWO_SM ? 2 : 1;                // cta_group of every tcgen05 instruction
   static_assert(BNT == BN || (!TWO_SM && BNT % 16 == 0 && BNT >= 32), "tile width");
-  // 64-wide tiles keep A's two TF32 parts in tensor memory (the MMAs read A
-  // from there, B from shared memory): each stage then moves a third less
-  // through shared memory, whose bandwidth the narrow tile's stages are
-  // bound by
+  // narrow tiles keep A's two TF32 parts in tensor memory (the MMAs read A
+  // from there, B from shared memory): a stage then holds a third less, so
+  // more stages fit, and the A residual never passes through shared memory
   constexpr bool A_TM = !TWO_SM && BNT != BN;
   static_assert(!A_TM || BK == 32, "A in tensor memory: 32-wide slices");
   using S = Slice<BK, TWO_SM ? 2 : 1, BNT, A_TM>;
@@ -751,22 +753,42 @@ struct Plan {
 Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   Plan pl{};
   pl.form = (want != kSingle && pairs > 0) ? want : (int)kSingle;
-  // 64-wide tiles (single CTAs) for N <= 64, so that the MMAs compute no
-  // columns beyond N -- a 256-wide tile would spend three quarters of its
-  // tensor-core work on them (16384 x 64 x 4096: 89.7 us against 149) --
-  // and for problems with little 256-wide work: at most 48 wide tiles and
-  // tiles x K at most 32 x 2048, where most SMs would get a slice of a split
-  // tile each. Measured on GB300 (us, 64-wide against 256-wide): 512^3 22.5 /
-  // 45.1, 1024^3 34.9 / 44.5, 512 x 512 x 8192 58.5 / 92.6, 1024 x 1024 x 2048
-  // 53.6 / 53.9; past either bound the wide tile wins: 1024 x 1024 x 4096
-  // 90.0 / 68.1, 2048 x 1024 x 1024 (64 tiles) 49.2 / 45.1, 1024 x 1024 x
-  // 16384 314 / 179.
-  constexpr long long kNarrowMaxWideTiles = 48, kNarrowMaxTileK = 32LL * 2048;
+  // The tile's width in N. Narrow tiles run on single CTAs with A's parts in
+  // tensor memory; per stage they issue as many MMAs as the wide tile for a
+  // quarter (64) or half (128) of its work, and with few tiles the schedule
+  // splits each tile along K over many CTAs, whose partial tiles one CTA then
+  // adds up. Measured on GB300 (us; 64 / 128 / 256 wide):
+  //   * N <= 64: 64 wide, so that the MMAs compute no columns beyond N
+  //     (16384 x 64 x 4096: 81 against 149 with 256-wide tiles);
+  //   * few 128-wide tiles for the K they have -- (sms / tiles)^2 > kiters / 2
+  //     with kiters 32-wide slices, the fix-up's partial tiles per tile
+  //     (sms / tiles) against the main loop's slices per CTA (tiles x kiters
+  //     / sms): 64 wide, as more, smaller tiles keep the fix-up short:
+  //     512^3 17.6 / 23.9, 300 x 520 x 4096 33.0 / 40.3; but 512 x 512 x 8192
+  //     53.5 / 48.9;
+  //   * otherwise 128 wide for N <= 128 (16384 x 128 x 4096: 88.5 against
+  //     140; 8192 x 96 x 4096: 57.3 against 90.2) and, below two waves of
+  //     256-wide tiles (where the wide schedule splits most of them), while
+  //     their work is at most 48 slices of 32 per CTA: 1024^3 30.4 / 26.8, 1024 x
+  //     1024 x 2048 47.1 / 36.2, 1024 x 1024 x 4096 - / 55.3 / 64.1, 2048 x
+  //     1024 x 1024 - / 33.3 / 41.1, 8191 x 1000 x 777 - / 98.5 / 105.7;
+  //   * beyond that 256 wide: 2048^3 (54 slices per CTA) 84.9 against 79.6,
+  //     1024 x 1024 x 16384 (108) 181.0 against 172.4.
+  const long long kiters32 = ceil_div_nn(K, 32);
+  const long long tiles_mid = (long long)ceil_div_nn(M, BM) * ceil_div_nn(N, BN_MID);
   const long long wide_tiles = (long long)ceil_div_nn(M, BM) * ceil_div_nn(N, BN);
-  pl.bn = (N <= BN_NARROW ||
-           (wide_tiles <= kNarrowMaxWideTiles && wide_tiles * K <= kNarrowMaxTileK))
-              ? BN_NARROW
-              : BN;
+  // (the products are formed only below these bounds, so they cannot overflow)
+  const bool few_mid_tiles =
+      tiles_mid < 2LL * sms && 2LL * sms * sms > kiters32 * tiles_mid * tiles_mid;
+  constexpr long long kMidMaxSlicesPerCta = 48;
+  const bool little_wide_work =
+      wide_tiles < 2LL * sms && wide_tiles * kiters32 <= kMidMaxSlicesPerCta * sms;
+  if (N <= BN_NARROW || few_mid_tiles)
+    pl.bn = BN_NARROW;
+  else if (N <= BN_MID || little_wide_work)
+    pl.bn = BN_MID;
+  else
+    pl.bn = BN;
   if (pl.bn != BN) pl.form = kSingle;
   // schedule: whole tiles, then the last one to two waves split along K. In
   // the pair form a schedule unit is two vertically adjacent tiles (a tile
@@ -775,9 +797,9 @@ Plan make_plan(int M, int N, int K, int want, int pairs, int sms) {
   // the k-slice width (see Slice). The two-SM form always takes 32: its
   // stages halve the per-stage hand-offs between the CTAs of a pair
   // (measured at 4096^3: 265 against 158 TFLOP/s with 16).
-  // 64-wide tiles also take 32: their stages carry a quarter of the MMA work,
-  // so the per-stage hand-offs dominate (measured at 16384 x 64 x 4096: 89.7
-  // against 106.8 us with 16-wide slices)
+  // Narrow tiles also take 32: their stages carry a quarter or half of the
+  // MMA work, so the per-stage hand-offs dominate (measured at 16384 x 64 x
+  // 4096: 89.7 against 106.8 us with 16-wide slices)
   auto slice_width = [K, &pl](int f) {
     return (f == kTwoSmPair || K < 1024 || pl.bn != BN) ? 32 : 16;
   };
@@ -888,6 +910,7 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
           cudaFuncSetAttribute(gemm_kernel<kSingle, 32>, attr, SMEM_BYTES) != cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kSingle, 32, BN_NARROW>, attr, SMEM_BYTES) !=
               cudaSuccess ||
+          cudaFuncSetAttribute(gemm_kernel<kSingle, 32, BN_MID>, attr, SMEM_BYTES) != cudaSuccess ||
           cudaFuncSetAttribute(gemm_kernel<kTwoSmPair, 32>, attr, SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return SGEMM_ERR_LAUNCH;
@@ -1014,12 +1037,15 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
     lc.stream = stream;
     lc.attrs = la;
     lc.numAttrs = CL == 2 ? 2 : 1;
+    using x3::BN_MID;
     using x3::BN_NARROW;
     cudaError_t e;
     if (CL == 2)  // the two-SM form always runs 32-wide slices (make_plan)
       e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kTwoSmPair, 32>, p, mA, mB);
-    else if (bn == BN_NARROW)  // 64-wide tiles always run 32-wide slices (make_plan)
+    else if (bn == BN_NARROW)  // narrow tiles always run 32-wide slices (make_plan)
       e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 32, BN_NARROW>, p, mA, mB);
+    else if (bn == BN_MID)
+      e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 32, BN_MID>, p, mA, mB);
     else if (bk == 16)
       e = cudaLaunchKernelEx(&lc, x3::gemm_kernel<x3::kSingle, 16>, p, mA, mB);
     else

@@ -99,17 +99,23 @@ def test_sweep_integer_bit_exact(n):
 
 
 def test_slice_width_follows_k(kernel_form):
-    # single CTAs with 256-wide tiles (17 x 6 of them: 54 tile pairs, fewer
-    # than the 76 clusters, so the pair form falls back): BK = 32 (two
-    # stages) below K = 1024, BK = 16 (four stages) from there
-    H.check_sampled(Workload("x3k", 2100, 1300, 1023, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
+    # single CTAs with 256-wide tiles (40 x 6 of them, more than 48 slices of
+    # 32 per CTA; 120 tile pairs, fewer than two waves of the 76 clusters, so
+    # the pair form falls back): BK = 32 (two stages) below K = 1024, BK = 16
+    # (four stages) from there
+    H.check_sampled(Workload("x3k", 5000, 1300, 1023, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
                     fn=X3)
     assert "128x256x32_s2" in binding.sgemm_last_config()
-    H.check_sampled(Workload("x3k", 2100, 1300, 1024, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
+    H.check_sampled(Workload("x3k", 5000, 1300, 1024, 1.0, 0.5, "int3", 38), rows=8, elements=1024,
                     fn=X3)
     assert "128x256x16_s4" in binding.sgemm_last_config()
-    # at most 48 wide tiles: 64-wide tiles, BK = 32 at any K (six stages: A's parts sit in tensor memory)
+    # little 256-wide work: 128-wide tiles, BK = 32 at any K (four stages:
+    # A's parts sit in tensor memory); few 128-wide tiles: 64-wide tiles, six
+    # stages
     for K in (1023, 1024):
+        H.check_sampled(Workload("x3k", 2000, 300, K, 1.0, 0.5, "int3", 38), rows=16, elements=2048,
+                        fn=X3)
+        assert "128x128x32_s4" in binding.sgemm_last_config()
         H.check_against_oracle(Workload("x3k", 200, 300, K, 1.0, 0.5, "int3", 38), fn=X3)
         assert "128x64x32_s6" in binding.sgemm_last_config()
     # whole waves of tile pairs at K = 1024: the two-SM form keeps BK = 32

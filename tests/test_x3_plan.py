@@ -3,7 +3,8 @@ runs, the k-slice width, the stages and the persistent schedule. The pair
 form falls back to single CTAs when the device keeps no CTA pairs resident or
 when every tile would be split along K; the two-SM form always takes 32-wide
 slices (three stages of half B tiles), single CTAs 16 from K = 1024 up and 32
-below; N <= 64 takes 64-wide tiles on single CTAs with 32-wide slices. The
+below; N <= 64 takes 64-wide tiles and N <= 128 (or little 256-wide work)
+128-wide tiles, on single CTAs with 32-wide slices. The
 GB300 figures (152 SMs, 76 resident pairs) are the ones the GPU runs report in
 sgemm_last_config()."""
 import pytest
@@ -46,11 +47,12 @@ def test_pairs_fall_back_without_resident_pairs():
 
 @pytest.mark.parametrize("K, bk, stages", [(1023, 32, 2), (1024, 16, 4), (777, 32, 2), (16384, 16, 4)])
 def test_single_cta_slice_width_follows_k(K, bk, stages):
-    p = plan(2100, 2600, K, SINGLE)      # 17 x 11 wide tiles
+    p = plan(4200, 2600, K, SINGLE)      # 33 x 11 wide tiles, over 48 slices of 32 per CTA
     assert (p["bn"], p["bk"], p["stages"], p["kiters"]) == (256, bk, stages, (K + bk - 1) // bk)
 
 
 def test_two_sm_form_keeps_32_wide_slices_at_any_k():
+    # 304 wide tiles: two waves of them, so 256-wide tiles at any K
     for K in (64, 1023, 1024, 8192):
         p = plan(128 * 2 * 76 * 2, 256, K, PAIR)
         assert (p["form"], p["bk"], p["stages"]) == (PAIR, 32, 3), K
@@ -91,27 +93,57 @@ def test_narrow_tiles_for_n_up_to_64(N, form):
         assert p["dp_units"] + p["split_units"] == 128
 
 
-def test_wide_tiles_from_n_65_with_more_than_48_of_them():
-    for N in (65, 96, 256, 4096):
-        assert plan(16384, N, 4096, SINGLE)["bn"] == 256, N   # at least 128 wide tiles
-    assert plan(2048, 2048, 2048, SINGLE)["bn"] == 256      # 128 wide tiles
-    assert plan(6272, 256, 512, SINGLE)["bn"] == 256        # 49 wide tiles
+def test_128_wide_tiles_up_to_n_128():
+    # 65 <= N <= 128: 128-wide tiles (a 256-wide tile would compute at least
+    # half its columns beyond N); A's parts in tensor memory, four 48 KB stages
+    for N in (65, 96, 128):
+        p = plan(16384, N, 4096, PAIR)
+        assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 128, 32, 4), N
 
 
-@pytest.mark.parametrize("M, N, K", [(512, 512, 512), (1024, 1024, 1024), (1536, 768, 1024),
-                                     (6144, 256, 512), (300, 520, 4096), (512, 512, 8192),
-                                     (1024, 1024, 2048)])
-def test_narrow_tiles_for_little_wide_work(M, N, K):
-    # at most 48 wide tiles and wide tiles x K at most 32 x 2048
+@pytest.mark.parametrize("M, N, K", [(1024, 1024, 1024), (1536, 768, 1024), (6144, 256, 512),
+                                     (512, 512, 8192), (1024, 1024, 2048), (1024, 1024, 4096),
+                                     (2048, 1024, 1024), (8191, 1000, 777), (6272, 256, 512)])
+def test_128_wide_tiles_for_little_wide_work(M, N, K):
+    # the 256-wide work is at most 48 slices of 32 per CTA (wide tiles x
+    # ceil(K / 32) <= 48 x 152), and the 128-wide tiles are not few
+    p = plan(M, N, K, PAIR)
+    assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 128, 32, 4)
+
+
+@pytest.mark.parametrize("M, N, K", [(512, 512, 512), (300, 520, 4096), (256, 256, 256),
+                                     (200, 300, 1024), (1024, 1024, 32), (128, 128, 128)])
+def test_64_wide_tiles_when_128_wide_tiles_are_few(M, N, K):
+    # (sms / tiles)^2 > ceil(K / 32) / 2 with 128-wide tiles: each would be
+    # split along K over so many CTAs that adding up their partial tiles
+    # outweighs the main loop
     p = plan(M, N, K, PAIR)
     assert (p["form"], p["bn"], p["bk"], p["stages"]) == (SINGLE, 64, 32, 6)
+    tiles = -(-M // 128) * -(-N // 128)
+    assert 2 * SMS * SMS > -(-K // 32) * tiles * tiles
 
 
-@pytest.mark.parametrize("M, N, K", [(1024, 1024, 4096), (1024, 1024, 16384), (512, 2048, 4096),
-                                     (1536, 1024, 3072), (2048, 1024, 1024), (1024, 1024, 3072)])
-def test_wide_tiles_past_either_bound(M, N, K):
+@pytest.mark.parametrize("M, N, K", [(2048, 2048, 2048), (1024, 1024, 16384), (16384, 129, 4096),
+                                     (16384, 4096, 4096), (3072, 2048, 1536)])
+def test_256_wide_tiles_past_48_slices_per_cta(M, N, K):
+    # more than 48 slices of 32 of 256-wide work per CTA
+    assert -(-M // 128) * -(-N // 256) * -(-K // 32) > 48 * SMS
     assert plan(M, N, K, SINGLE)["bn"] == 256
 
+
+@pytest.mark.parametrize("M, N, K", [(128 * 2 * 76 * 2, 256, 64), (128 * 2 * 76, 512, 32),
+                                     (4096, 4096, 32)])
+def test_256_wide_tiles_from_two_waves_of_them(M, N, K):
+    # at least 2 x 152 wide tiles, however short K
+    assert -(-M // 128) * -(-N // 256) >= 2 * SMS
+    assert plan(M, N, K, SINGLE)["bn"] == 256
+
+
+def test_tile_width_rule_has_no_overflow_at_the_largest_sizes():
+    big = 2 ** 31 - 1
+    for (M, N, K) in [(big, 64, 64), (65536, big // 4, 32), (64, 64, big)]:
+        st, p = binding.sgemm_3xtf32_plan(M, N, K, PAIR, PAIRS, SMS)
+        assert st == 0 and p["bn"] in (64, 128, 256), (M, N, K)
 
 
 def test_pair_form_splits_the_last_two_waves_when_the_last_is_thin():
