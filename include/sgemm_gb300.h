@@ -134,8 +134,12 @@ int sgemm_3xtf32_set_kernel_form(int form);
  * out (9 ints) = {form that runs, k-slice width, stages, CTAs, schedule
  * units (a CTA pair each in the pair forms), whole-tile units, K-split units,
  * k-slices, tile width in N}. The pair form falls back to single CTAs when
- * pairs == 0 or when every tile would be split along K; N <= 64 takes 64-wide
- * tiles (single CTAs) instead of 256-wide ones. Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM unless
+ * pairs == 0 or when every tile would be split along K. The tile width: 64
+ * for N <= 64 and for problems of few 128-wide tiles ((sms / tiles)^2 >
+ * ceil(K / 32) / 2), 128 for N <= 128 and for fewer than two waves of
+ * 256-wide tiles with at most 48 slices of 32 of their work per SM, else 256;
+ * the 64- and 128-wide tiles run on single CTAs with 32-wide slices.
+ * Returns SGEMM_OK, SGEMM_ERR_INVALID_DIM unless
  * M, N, K >= 1 (only such problems launch the GEMM kernel), or
  * SGEMM_ERR_INVALID_VALUE for another form, pairs < 0, sms < 1 or a NULL out.
  * The pages are silent (no tensor-core kernel, one CTA per tile).
