@@ -1,5 +1,5 @@
 // probe.cu -- sgemm_diag_tf32_mma_rate(): the TF32 tensor-core throughput of
-// this GPU, measured. The 3xTF32 path is judged against it (three TF32
+// this GPU, measured. The 3xTF32 path is measured against it (three TF32
 // products per FP32 product), so its roofline rests on this device rather
 // than on a nominal figure.
 //

@@ -235,7 +235,7 @@ int sgemm_last_config(char* buf, int len);
  * split partial, 4 = CTA rendezvous, 5 = the two CTAs of a two-SM pair of
  * sgemm_3xtf32 got different tensor-memory columns; none of them is a device
  * fault, and the context stays usable). SGEMM_ERR_LAUNCH if synchronising
- * fails. `detail` extends the survey's one-argument form of this call: the
+ * fails. `detail` extends the one-argument form this call would otherwise have: the
  * status alone cannot say which wait gave up. The pages are silent (their
  * kernels have no bounded waits and report nothing).
  */
