@@ -144,6 +144,14 @@ static_assert(BN % 16 == 0 && BN <= 256 && BM == 128, "MMA shape");
 // the narrow tiles: 64 wide for N <= 64 and problems of few tiles, 128 wide
 // for N <= 128 and problems with little 256-wide work (make_plan)
 constexpr int BN_NARROW = 64, BN_MID = 128;
+// the host's stage count (plan, shared-memory layout) is the kernel's, for
+// every instantiated tile
+static_assert(stages_of(kSingle, 16, BN) == Slice<16>::ST &&
+                  stages_of(kSingle, 32, BN) == Slice<32>::ST &&
+                  stages_of(kTwoSmPair, 32, BN) == Slice<32, 2>::ST &&
+                  stages_of(kSingle, 32, BN_NARROW) == Slice<32, 1, BN_NARROW, true>::ST &&
+                  stages_of(kSingle, 32, BN_MID) == Slice<32, 1, BN_MID, true>::ST,
+              "stage counts");
 
 struct Barriers {
   uint64_t full[kMaxStages];   // TMA transaction bytes of one stage (the raw tiles)
