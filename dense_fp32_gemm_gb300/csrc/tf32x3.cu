@@ -133,7 +133,8 @@ enum Form : int { kSingle = 1, kTwoSmPair = 2 };
 // Stages of a (form, k-slice width, tile width): Slice<>::ST, for the host.
 constexpr int stages_of(int form, int bk, int bnt) {
   const bool a_tmem = form == kSingle && bnt != BN;  // the kernel's A_TM
-  const int stage = (a_tmem ? 1 : 2) * BM * bk * 4 + 2 * (bnt / (form == kTwoSmPair ? 2 : 1)) * bk * 4;
+  const int b_rows = bnt / (form == kTwoSmPair ? 2 : 1);
+  const int stage = (a_tmem ? 1 : 2) * BM * bk * 4 + 2 * b_rows * bk * 4;
   return kStageRegion / stage < kMaxStages ? kStageRegion / stage : kMaxStages;
 }
 constexpr int EPI_THREADS = 128;          // warps 2-5
@@ -883,7 +884,8 @@ SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float* A, int
   const bool reads_ab = (K > 0 && alpha != 0.f);
   if (C == nullptr || (reads_ab && (A == nullptr || B == nullptr))) return SGEMM_ERR_NULL_PTR;
   if ((reinterpret_cast<uintptr_t>(C) & 3u) ||
-      (reads_ab && ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))))
+      (reads_ab &&
+       ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(B) & 3u))))
     return SGEMM_ERR_MISALIGNED;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
