@@ -98,6 +98,25 @@ def test_sweep_integer_bit_exact(n):
     H.check_sampled(WORKLOADS[f"sweep{n}_int"], rows=4, elements=512, fn=X3)
 
 
+@pytest.mark.parametrize("dist", ["int3", "uniform"])
+@pytest.mark.parametrize("shape, width", [((6000, 100, 1100), 128), ((3000, 300, 777), 128),
+                                          ((4100, 127, 2049), 128), ((5000, 1000, 200), 128),
+                                          ((3000, 64, 1100), 64), ((700, 33, 3000), 64)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_narrow_tiles_ragged_and_misaligned(shape, width, dist):
+    # the 64- and 128-wide tiles (A's parts in tensor memory) on a ragged last
+    # tile row, tile column and k-slice; K-split tiles everywhere, and whole
+    # tiles too at 5000 x 1000 x 200 (two waves of 128-wide tiles). First with
+    # every pointer off 16 bytes and padded leading dimensions (A then copied,
+    # C by scalar accesses) and beta = 0, then aligned with beta != 0
+    M, N, K = shape
+    for beta, offsets, pads in ((0.0, (1, 2, 3), (1, 2, 3)), (-0.5, (0, 0, 0), (4, 0, 4))):
+        w = Workload("x3narrow", M, N, K, 1.25, beta, dist, 43, lda=K + pads[0], ldb=N + pads[1],
+                     ldc=N + pads[2])
+        H.check_against_oracle(w, offsets=offsets, fn=X3)
+        assert f"3xtf32_tcgen05_128x{width}x32" in binding.sgemm_last_config(), (shape, beta)
+
+
 def test_slice_width_follows_k(kernel_form):
     # single CTAs with 256-wide tiles (40 x 6 of them, more than 48 slices of
     # 32 per CTA; 120 tile pairs, fewer than two waves of the 76 clusters, so
