@@ -7,6 +7,7 @@ below; N <= 64 takes 64-wide tiles and N <= 128 (or little 256-wide work)
 128-wide tiles, on single CTAs with 32-wide slices. The
 GB300 figures (152 SMs, 76 resident pairs) are the ones the GPU runs report in
 sgemm_last_config()."""
+import numpy as np
 import pytest
 
 from dense_fp32_gemm_gb300 import binding
@@ -162,3 +163,22 @@ def test_below_two_waves_of_pairs_single_ctas_run():
     # one-wave split)
     p = plan(3072, 2048, 1536, PAIR)
     assert (p["form"], p["dp_units"]) == (SINGLE, 0)
+
+
+def test_narrow_tiles_fit_tensor_memory_and_shared_memory():
+    # narrow tiles: two accumulators of the tile's width plus a 64-column A
+    # slot (32 raw + 32 residual TF32 columns) per stage within the 512 TMEM
+    # columns; stages of A's raw tile and B's two parts within the 192 KB ring
+    rng = np.random.default_rng(5)
+    seen = set()
+    for _ in range(2000):
+        M, N, K = (int(x) for x in rng.integers(1, 20000, 3))
+        p = plan(M, N, K, PAIR)
+        seen.add(p["bn"])
+        if p["bn"] == 256:
+            continue
+        assert (p["form"], p["bk"]) == (SINGLE, 32), (M, N, K)
+        assert 2 * p["bn"] + 64 * p["stages"] <= 512, (M, N, K, p)
+        stage_bytes = 128 * 32 * 4 + 2 * p["bn"] * 32 * 4
+        assert p["stages"] * stage_bytes <= 192 * 1024 and p["stages"] >= 3, (M, N, K, p)
+    assert seen == {64, 128, 256}
