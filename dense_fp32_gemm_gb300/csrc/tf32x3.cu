@@ -22,12 +22,13 @@
 //      padded to a multiple of 4 floats for TMA); A is read where it is when
 //      its rows are 16-byte aligned, else copied there too;
 //   2. the GEMM kernel (one CTA of 10 warps per SM, persistent over 128 x 256
-//      tiles): warp 0 issues TMA loads of the raw A and B^T tiles of each
-//      k-slice (swizzled) into a ring of stages; warps 6-9 write the
-//      residual tiles A_lo, B_lo beside them in the same stage; warp 1 owns
-//      two 256-column TMEM accumulators and issues, per 8-wide k-step, the
-//      three tcgen05.mma.kind::tf32 products; warps 2-5 read an accumulator
-//      back with tcgen05.ld and apply alpha * acc + beta * C.
+//      tiles, or the narrow tiles below): warp 0 issues TMA loads of the raw
+//      A and B^T tiles of each k-slice (swizzled) into a ring of stages;
+//      warps 6-9 write the residual tiles A_lo, B_lo beside them in the same
+//      stage; warp 1 owns two TMEM accumulators of the tile's width and
+//      issues, per 8-wide k-step, the three tcgen05.mma.kind::tf32 products;
+//      warps 2-5 read an accumulator back with tcgen05.ld and apply
+//      alpha * acc + beta * C.
 //
 // Kernel forms (sgemm_3xtf32_set_kernel_form):
 //   * two-SM pairs (the default where the device co-schedules CTA pairs and
